@@ -1,0 +1,417 @@
+// Block-scaled FP8 (E4M3) GEMM on the 5th-generation tensor cores (sm_103a).
+//
+//   D[r][c] = bf16( sum_g  sa(g,r) * sb(g,c) * P_g[r][c] ),
+//   P_g = A[:, 128g:128g+128] * B[:, 128g:128g+128]^T   (exact FP8 products,
+//                                                         fp32 sums, tensor cores)
+//
+// One kernel serves the three products of a linear layer (Jet-RL, technical
+// summaries on gist.science, "Schéma de Quantification": FP8 GEMMs for the
+// forward pass and for DGrad / WGrad, 1x128 activation groups, 128x128
+// weight blocks, 1x128 and 128x1 groups for WGrad):
+//   Fprop  A = X codes [M][K],    sa = X's 1x128 scales,   B = W codes [N][K],
+//          sb = one scale per 128x128 weight block;
+//   Dgrad  A = dY codes [M][N],   sa = dY's 1x128 scales,  B = W^T codes [K][N],
+//          sb = one scale per 128x128 weight block;
+//   Wgrad  A = dY^T codes [N][M], sa = dY's 128x1 scales,  B = X^T codes [K][M],
+//          sb = X's 128x1 scales (one per output column and token group).
+// The scales are arbitrary fp32 values (amax / 448), not powers of two, so the
+// tensor core's own block scaling cannot apply them: each 128-wide group is
+// multiplied into a fresh TMEM partial and CUDA-core warps fold it into an
+// fp32 register accumulator with the group's scales ("promotion").
+//
+// Structure: persistent, one CTA per SM, 384 threads (3 warpgroups).
+//   warp 0, lane 0 : TMA producer   -- A and B tiles of one group per smem stage
+//   warp 1, lane 0 : MMA issuer     -- 4 x tcgen05.mma (K = 32 each) per group
+//                                      into one of two TMEM partial buffers
+//   warps 4..11    : promotion      -- two warpgroups, each 128 rows x BN/2
+//                                      columns; tcgen05.ld the partial, free the
+//                                      buffer, acc += partial * sa * sb; bf16
+//                                      epilogue straight from registers
+// Registers are rebalanced with setmaxnreg: the control warpgroup drops to 40
+// per thread and the promotion warpgroups rise to 232 (128*40 + 256*232 =
+// 64512 = 384 threads * 168, the launch allocation).
+// Tile BM = 128 rows x BN (256 or 128) columns; one pipeline stage per
+// 128-wide K group (the scale granularity).  Every wait is bounded: a
+// wait that runs out sets the device error word, the CTA drains its copies
+// and MMAs in flight, frees its tensor memory and exits.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "internal.cuh"
+#include "ptx.cuh"
+
+namespace jetfp8 {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 128;                  // one scale group
+constexpr int NUM_THREADS = 384;
+constexpr int PRODUCER_WARP = 0;
+constexpr int MMA_WARP = 1;
+constexpr int FIRST_PROMO_WARP = 4;
+constexpr uint32_t CTRL_REGS = 40;
+constexpr uint32_t PROMO_REGS = 232;
+static_assert(128 * CTRL_REGS + 256 * PROMO_REGS <= NUM_THREADS * 168, "register split exceeds the launch allocation");
+constexpr int GROUP_M = 16;              // tile rasterisation: m-tiles per band
+constexpr uint64_t WAIT_TIMEOUT_NS = 2000000000ull;   // 2 s
+
+struct KernelArgs {
+    const float *sa;
+    const float *sb;
+    int64_t sb_stride_g;
+    int64_t sb_stride_c;
+    __nv_bfloat16 *d;
+    uint32_t *err;
+    int32_t rows, cols, groups;
+    int32_t tiles_m, tiles_n;
+};
+
+template <int BN, int STAGES>
+struct Smem {
+    static constexpr uint32_t A_BYTES = BM * BK;
+    static constexpr uint32_t B_BYTES = BN * BK;
+    static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr uint32_t TILES = STAGES * STAGE_BYTES;
+    static constexpr uint32_t BAR_OFF = TILES;
+    // full[S], empty[S], tfull[2], tempty[2], mma_done, tmem holder, abort flag
+    static constexpr uint32_t CTRL_BYTES = (2 * STAGES + 5) * 8 + 16;
+    static constexpr uint32_t TOTAL = 1024 /* alignment slack */ + TILES + CTRL_BYTES;
+};
+
+__device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int &tm, int &tn)
+{
+    const int per_band = GROUP_M * tiles_n;
+    const int band = tile / per_band;
+    const int first_m = band * GROUP_M;
+    const int band_m = min(tiles_m - first_m, GROUP_M);
+    const int in_band = tile - band * per_band;
+    tm = first_m + in_band % band_m;
+    tn = in_band / band_m;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+template <int BN, int STAGES, bool SB_PER_COLUMN>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+            const KernelArgs args)
+{
+    using L = Smem<BN, STAGES>;
+    constexpr int COLS_PER_WG = BN / 2;          // columns per promotion warpgroup
+    constexpr int CHUNKS = COLS_PER_WG / 32;     // tcgen05.ld x32 per group
+    constexpr uint32_t TMEM_COLS = 2 * BN;       // two partial buffers
+    constexpr uint32_t IDESC = ptx::idesc_e4m3_f32(BM, BN);
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sA = smem;
+    uint8_t *sB = smem + STAGES * L::A_BYTES;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::BAR_OFF);
+    uint64_t *empty = full + STAGES;
+    uint64_t *tfull = empty + STAGES;
+    uint64_t *tempty = tfull + 2;
+    uint64_t *mma_done = tempty + 2;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(mma_done + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int num_tiles = args.tiles_m * args.tiles_n;
+    const int G = args.groups;
+
+    if (warp == PRODUCER_WARP) {
+        if (lane == 0) {
+            for (int s = 0; s < STAGES; ++s) {
+                ptx::mbar_init(&full[s], 1);
+                ptx::mbar_init(&empty[s], 1);
+            }
+            for (int b = 0; b < 2; ++b) {
+                ptx::mbar_init(&tfull[b], 1);
+                ptx::mbar_init(&tempty[b], 8);   // one arrival per promotion warp (8 warps)
+            }
+            ptx::mbar_init(mma_done, 1);
+            *abort_flag = 0;
+            ptx::fence_mbar_init();
+            ptx::tma_prefetch_desc(&tmap_a);
+            ptx::tma_prefetch_desc(&tmap_b);
+        }
+        __syncwarp();
+        ptx::tmem_alloc(tmem_holder, TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    if (warp < FIRST_PROMO_WARP) {
+      ptx::setmaxnreg_dec<CTRL_REGS>();
+      if (warp == PRODUCER_WARP) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued_mask = 0, issued_parity = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+                int tm, tn;
+                tile_coords(tile, args.tiles_m, args.tiles_n, tm, tn);
+                for (int g = 0; g < G; ++g) {
+                    if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, args.err, ERRBIT_PRODUCER,
+                                        WAIT_TIMEOUT_NS)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::mbar_arrive_expect_tx(&full[stage], L::STAGE_BYTES);
+                    ptx::tma_load_2d(sA + stage * L::A_BYTES, &tmap_a, &full[stage], g * BK, tm * BM);
+                    ptx::tma_load_2d(sB + stage * L::B_BYTES, &tmap_b, &full[stage], g * BK, tn * BN);
+                    issued_mask |= 1u << stage;
+                    issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // drain: every copy this thread started must land before exit
+                for (int s = 0; s < STAGES; ++s)
+                    if (issued_mask & (1u << s))
+                        ptx::mbar_wait(&full[s], (issued_parity >> s) & 1u, nullptr, args.err, ERRBIT_DRAIN,
+                                       WAIT_TIMEOUT_NS);
+            }
+        }
+        __syncwarp();
+      } else if (warp == MMA_WARP) {
+        // ------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t it = 0;   // global group counter -> TMEM buffer / phase
+            bool ok = true;
+            const uint32_t a_base = ptx::smem_u32(sA);
+            const uint32_t b_base = ptx::smem_u32(sB);
+            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+                for (int g = 0; g < G; ++g, ++it) {
+                    const uint32_t buf = it & 1u;
+                    const uint32_t bphase = (it >> 1) & 1u;
+                    if (!ptx::mbar_wait(&tempty[buf], bphase ^ 1u, abort_flag, args.err, ERRBIT_MMA_TMEM,
+                                        WAIT_TIMEOUT_NS) ||
+                        !ptx::mbar_wait(&full[stage], phase, abort_flag, args.err, ERRBIT_MMA_SMEM,
+                                        WAIT_TIMEOUT_NS)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint64_t adesc = ptx::smem_desc_sw128_kmajor(a_base + stage * L::A_BYTES);
+                    const uint64_t bdesc = ptx::smem_desc_sw128_kmajor(b_base + stage * L::B_BYTES);
+                    const uint32_t d_tmem = tmem_base + buf * BN;
+#pragma unroll
+                    for (int j = 0; j < BK / 32; ++j)   // K = 32 bytes per instruction: +2 in the >>4 address field
+                        ptx::mma_f8(d_tmem, adesc + 2 * j, bdesc + 2 * j, IDESC, j > 0 ? 1u : 0u);
+                    ptx::mma_commit(&empty[stage]);
+                    ptx::mma_commit(&tfull[buf]);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // all MMAs issued by this thread complete before teardown
+            ptx::mma_commit(mma_done);
+            ptx::mbar_wait(mma_done, 0, nullptr, args.err, ERRBIT_DRAIN, WAIT_TIMEOUT_NS);
+        }
+        __syncwarp();
+      }
+    } else {
+        ptx::setmaxnreg_inc<PROMO_REGS>();
+        // ------------------------------------------------------ promotion
+        const int wg = (warp - FIRST_PROMO_WARP) >> 2;   // 0 or 1: column half of the tile
+        const int quarter = warp & 3;         // TMEM lanes 32*quarter .. +31
+        const int row_in_tile = quarter * 32 + lane;
+        uint32_t it = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+            int tm, tn;
+            tile_coords(tile, args.tiles_m, args.tiles_n, tm, tn);
+            const int row = tm * BM + row_in_tile;
+            const bool row_ok = row < args.rows;
+            const int col0 = tn * BN + wg * COLS_PER_WG;
+            const bool cols_ok = col0 < args.cols;
+            float acc[COLS_PER_WG];
+#pragma unroll
+            for (int i = 0; i < COLS_PER_WG; ++i)
+                acc[i] = 0.0f;
+
+            float sa_next = row_ok ? __ldg(args.sa + row) : 0.0f;
+            for (int g = 0; g < G; ++g, ++it) {
+                const uint32_t buf = it & 1u;
+                const uint32_t bphase = (it >> 1) & 1u;
+                const float sa = sa_next;
+                if (g + 1 < G)
+                    sa_next = row_ok ? __ldg(args.sa + static_cast<int64_t>(g + 1) * args.rows + row) : 0.0f;
+                float w_blk = 0.0f;
+                const float *sbg = args.sb + static_cast<int64_t>(g) * args.sb_stride_g;
+                if (!SB_PER_COLUMN)
+                    w_blk = sa * (cols_ok ? __ldg(sbg + static_cast<int64_t>(col0 >> 7) * args.sb_stride_c) : 0.0f);
+
+                if (!ptx::mbar_wait(&tfull[buf], bphase, abort_flag, args.err, ERRBIT_PROMOTE, WAIT_TIMEOUT_NS)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + buf * BN +
+                                       wg * COLS_PER_WG;
+                uint32_t p[2][32];
+                ptx::tmem_ld_32x32b_x32(taddr, p[0]);
+                ptx::tmem_ld_wait(p[0]);
+#pragma unroll
+                for (int c = 0; c < CHUNKS; ++c) {
+                    uint32_t(&cur)[32] = p[c & 1];
+                    if (c + 1 < CHUNKS) {
+                        ptx::tmem_ld_32x32b_x32(taddr + (c + 1) * 32, p[(c + 1) & 1]);
+                    } else {
+                        // the whole partial is in registers: hand the buffer back
+                        ptx::tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0)
+                            ptx::mbar_arrive(&tempty[buf]);
+                    }
+                    if (SB_PER_COLUMN) {
+                        const float4 *sbv = reinterpret_cast<const float4 *>(sbg + col0 + c * 32);
+#pragma unroll
+                        for (int v = 0; v < 8; ++v) {
+                            const float4 s4 = cols_ok ? __ldg(sbv + v) : make_float4(0.f, 0.f, 0.f, 0.f);
+                            acc[c * 32 + 4 * v + 0] = fmaf(__uint_as_float(cur[4 * v + 0]), sa * s4.x, acc[c * 32 + 4 * v + 0]);
+                            acc[c * 32 + 4 * v + 1] = fmaf(__uint_as_float(cur[4 * v + 1]), sa * s4.y, acc[c * 32 + 4 * v + 1]);
+                            acc[c * 32 + 4 * v + 2] = fmaf(__uint_as_float(cur[4 * v + 2]), sa * s4.z, acc[c * 32 + 4 * v + 2]);
+                            acc[c * 32 + 4 * v + 3] = fmaf(__uint_as_float(cur[4 * v + 3]), sa * s4.w, acc[c * 32 + 4 * v + 3]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            acc[c * 32 + i] = fmaf(__uint_as_float(cur[i]), w_blk, acc[c * 32 + i]);
+                    }
+                    if (c + 1 < CHUNKS)
+                        ptx::tmem_ld_wait(p[(c + 1) & 1]);
+                }
+            }
+            if (!ok)
+                break;
+            if (row_ok && cols_ok) {
+                uint4 *dst = reinterpret_cast<uint4 *>(args.d + static_cast<int64_t>(row) * args.cols + col0);
+#pragma unroll
+                for (int v = 0; v < COLS_PER_WG / 8; ++v) {
+                    uint4 o;
+                    o.x = pack_bf16x2(acc[8 * v + 0], acc[8 * v + 1]);
+                    o.y = pack_bf16x2(acc[8 * v + 2], acc[8 * v + 3]);
+                    o.z = pack_bf16x2(acc[8 * v + 4], acc[8 * v + 5]);
+                    o.w = pack_bf16x2(acc[8 * v + 6], acc[8 * v + 7]);
+                    dst[v] = o;
+                }
+            }
+        }
+    }
+
+    // ---------------------------------------------------------- teardown
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    if (warp == PRODUCER_WARP)
+        ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+template <int BN, int STAGES, bool SB_PER_COLUMN>
+cudaError_t launch_variant(const GemmProblem &p, const DeviceInfo &dev, const CUtensorMap &ta, const CUtensorMap &tb,
+                           cudaStream_t stream)
+{
+    using L = Smem<BN, STAGES>;
+    auto kern = gemm_kernel<BN, STAGES, SB_PER_COLUMN>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(L::TOTAL));
+    if (e != cudaSuccess)
+        return e;
+    KernelArgs a;
+    a.sa = p.sa;
+    a.sb = p.sb;
+    a.sb_stride_g = p.sb_stride_g;
+    a.sb_stride_c = p.sb_stride_c;
+    a.d = static_cast<__nv_bfloat16 *>(p.d);
+    a.err = dev.err_word;
+    a.rows = static_cast<int32_t>(p.rows);
+    a.cols = static_cast<int32_t>(p.cols);
+    a.groups = static_cast<int32_t>(p.kdim / BK);
+    a.tiles_m = static_cast<int32_t>((p.rows + BM - 1) / BM);
+    a.tiles_n = static_cast<int32_t>((p.cols + BN - 1) / BN);
+    const int tiles = a.tiles_m * a.tiles_n;
+    const int grid = tiles < dev.sm_count ? tiles : dev.sm_count;
+    kern<<<grid, NUM_THREADS, L::TOTAL, stream>>>(ta, tb, a);
+    return cudaGetLastError();
+}
+
+CUresult encode_operand(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap *map, const uint8_t *ptr,
+                        int64_t rows, int64_t kdim, int box_rows)
+{
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(kdim), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(kdim)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const GemmProblem &p, const DeviceInfo &dev, PFN_cuTensorMapEncodeTiled_v12000 encode,
+                        cudaStream_t stream)
+{
+    // Wide tiles unless they would leave most SMs idle (small problems).
+    const int64_t tiles256 = ((p.rows + BM - 1) / BM) * ((p.cols + 255) / 256);
+    const bool wide = tiles256 >= dev.sm_count;
+    const int bn = wide ? 256 : 128;
+    CUtensorMap ta, tb;
+    if (encode_operand(encode, &ta, p.a, p.rows, p.kdim, BM) != CUDA_SUCCESS ||
+        encode_operand(encode, &tb, p.b, p.cols, p.kdim, bn) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    const bool per_col = p.sb_mode == ScaleB::PerColumn;
+    if (wide)
+        return per_col ? launch_variant<256, 4, true>(p, dev, ta, tb, stream)
+                       : launch_variant<256, 4, false>(p, dev, ta, tb, stream);
+    return per_col ? launch_variant<128, 6, true>(p, dev, ta, tb, stream)
+                   : launch_variant<128, 6, false>(p, dev, ta, tb, stream);
+}
+
+// ---------------------------------------------------------------------------
+// Watchdog self-test: one warp waits, bounded, on a barrier that nothing
+// completes, using the same routine as the GEMM's waits.
+// ---------------------------------------------------------------------------
+namespace {
+__global__ void watchdog_selftest_kernel(uint32_t *err, uint64_t timeout_ns)
+{
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(&bar, 1);
+        abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0)
+        ptx::mbar_wait(&bar, 0, &abort_flag, err, ERRBIT_SELFTEST, timeout_ns);
+    __syncthreads();
+}
+}  // namespace
+
+cudaError_t launch_watchdog_selftest(uint32_t *err_word, uint64_t timeout_ns, cudaStream_t stream)
+{
+    watchdog_selftest_kernel<<<1, 32, 0, stream>>>(err_word, timeout_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace jetfp8

@@ -1,0 +1,300 @@
+// Group-wise FP8 (E4M3) quantisers for sm_103a.
+//
+// Jet-RL (technical summaries on gist.science, "Schéma de Quantification"):
+// activations and gradients use 1x128 groups, weights 128x128 blocks, and the
+// WGrad operands 128x1 groups along the token axis ("1x128 et 128x1 pour
+// WGrad"), which the transposed quantiser writes out as 1x128 groups of the
+// transposed tensor.  Per group: amax = max |x|, s = amax / 448 (IEEE fp32
+// division), code = E4M3(RNE, saturating)(x / s) (IEEE fp32 division); a
+// zero group stores s = 0 and codes 0x00.
+//
+// All three kernels are HBM-streaming: 16-byte vector loads, warp-shuffle
+// amax reductions, and stores arranged so that every written sector is full.
+// Compiled without fast-math so that `/` is the correctly rounded IEEE
+// division and subnormals are kept.
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "internal.cuh"
+#include "ptx.cuh"
+
+namespace jetfp8 {
+namespace {
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8])
+{
+    f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
+    f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+    f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z);
+    f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+}
+
+__device__ __forceinline__ float absmax8(const float (&f)[8])
+{
+    float a = fabsf(f[0]);
+#pragma unroll
+    for (int i = 1; i < 8; ++i)
+        a = fmaxf(a, fabsf(f[i]));
+    return a;
+}
+
+// Codes for 4 consecutive values, little-endian in one word (value i in byte i).
+__device__ __forceinline__ uint32_t encode4(float a, float b, float c, float d, float s)
+{
+    const uint32_t lo = ptx::cvt_e4m3x2(a / s, b / s);
+    const uint32_t hi = ptx::cvt_e4m3x2(c / s, d / s);
+    return lo | (hi << 16);
+}
+
+__device__ __forceinline__ uint2 encode8(const float (&f)[8], float s)
+{
+    if (s == 0.0f)
+        return make_uint2(0u, 0u);
+    return make_uint2(encode4(f[0], f[1], f[2], f[3], s), encode4(f[4], f[5], f[6], f[7], s));
+}
+
+// ---------------------------------------------------------------------------
+// 1x128 groups along rows.  CTA tile: 32 rows x 8 groups (1024 columns).
+// Warp w owns rows w, w+8, w+16, w+24; each half-warp owns one group of a
+// row per step (16 lanes x 8 values).  Scales are staged in shared memory and
+// written group-major, 32 consecutive rows (128 bytes) per group.
+// ---------------------------------------------------------------------------
+constexpr int Q1_ROWS = 32;
+constexpr int Q1_GROUPS = 8;
+constexpr int Q1_THREADS = 256;
+
+__global__ void __launch_bounds__(Q1_THREADS)
+quantize_act_kernel(const uint4 *__restrict__ x, int64_t M, int64_t K, uint2 *__restrict__ q,
+                    float *__restrict__ s)
+{
+    __shared__ float s_tile[Q1_GROUPS][Q1_ROWS];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int half = lane >> 4, sub = lane & 15;
+    const int64_t G = K >> 7;
+    const int64_t m0 = static_cast<int64_t>(blockIdx.x) * Q1_ROWS;
+    const int64_t g0 = static_cast<int64_t>(blockIdx.y) * Q1_GROUPS;
+    const int64_t K8 = K >> 3;   // 16-byte chunks per bf16 row (8 codes per uint2 chunk as well)
+
+    uint4 v[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int64_t m = m0 + warp + 8 * i;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int64_t g = g0 + 2 * j + half;
+            if (m < M && g < G)
+                v[i][j] = __ldcs(x + m * K8 + g * 16 + sub);
+            else
+                v[i][j] = make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int64_t m = m0 + warp + 8 * i;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int64_t g = g0 + 2 * j + half;
+            float f[8];
+            unpack8(v[i][j], f);
+            float amax = absmax8(f);
+#pragma unroll
+            for (int o = 8; o >= 1; o >>= 1)
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            const float sc = amax / 448.0f;
+            const uint2 codes = encode8(f, sc);
+            if (m < M && g < G)
+                __stcs(q + m * K8 + g * 16 + sub, codes);
+            if (sub == 0)
+                s_tile[2 * j + half][warp + 8 * i] = sc;
+        }
+    }
+    __syncthreads();
+    {
+        const int gl = threadIdx.x >> 5, r = threadIdx.x & 31;
+        const int64_t g = g0 + gl, m = m0 + r;
+        if (g < G && m < M)
+            s[g * M + m] = s_tile[gl][r];
+    }
+}
+
+// ---------------------------------------------------------------------------
+// 128x1 groups along rows (tokens) of each column, written transposed.
+// CTA tile: 128 rows x 64 columns of bf16 staged in shared memory (16-byte
+// chunks XOR-swizzled by row so that both the row-wise fill and the
+// column-wise reads are bank-conflict free).  Warp w reads column
+// 32*(w&1)+lane over rows 32*(w>>1) .. +31; the four row quarters combine
+// their amax through shared memory; each thread then writes 32 contiguous
+// codes (one full 32-byte sector) of its output row.
+// ---------------------------------------------------------------------------
+constexpr int Q2_ROWS = 128;
+constexpr int Q2_COLS = 64;
+constexpr int Q2_THREADS = 256;
+
+__global__ void __launch_bounds__(Q2_THREADS)
+quantize_act_t_kernel(const uint4 *__restrict__ x, int64_t M, int64_t C, uint8_t *__restrict__ qt,
+                      float *__restrict__ st)
+{
+    __shared__ uint4 tile[Q2_ROWS][Q2_COLS / 8];
+    __shared__ float s_amax[4][Q2_COLS];
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const int64_t m0 = static_cast<int64_t>(blockIdx.x) * Q2_ROWS;
+    const int64_t c0 = static_cast<int64_t>(blockIdx.y) * Q2_COLS;
+    const int64_t C8 = C >> 3;
+
+    uint4 v[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        const int idx = p * Q2_THREADS + t;
+        const int r = idx >> 3, ch = idx & 7;
+        v[p] = __ldcs(x + (m0 + r) * C8 + (c0 >> 3) + ch);
+    }
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        const int idx = p * Q2_THREADS + t;
+        const int r = idx >> 3, ch = idx & 7;
+        tile[r][ch ^ (r & 7)] = v[p];
+    }
+    __syncthreads();
+
+    const int c = 32 * (warp & 1) + lane;   // column within the tile
+    const int qd = warp >> 1;               // row quarter
+    const int chunk = c >> 3, elem = c & 7;
+    float f[32];
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const int r = 32 * qd + i;
+        const uint16_t *row = reinterpret_cast<const uint16_t *>(&tile[r][0]);
+        f[i] = __uint_as_float(static_cast<uint32_t>(row[((chunk ^ (r & 7)) << 3) + elem]) << 16);
+        amax = fmaxf(amax, fabsf(f[i]));
+    }
+    s_amax[qd][c] = amax;
+    __syncthreads();
+    amax = fmaxf(fmaxf(s_amax[0][c], s_amax[1][c]), fmaxf(s_amax[2][c], s_amax[3][c]));
+    const float sc = amax / 448.0f;
+
+    uint32_t w[8];
+    if (sc == 0.0f) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            w[i] = 0u;
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            w[i] = encode4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3], sc);
+    }
+    uint4 *dst = reinterpret_cast<uint4 *>(qt + (c0 + c) * M + m0 + 32 * qd);
+    __stcs(dst, make_uint4(w[0], w[1], w[2], w[3]));
+    __stcs(dst + 1, make_uint4(w[4], w[5], w[6], w[7]));
+    if (qd == 0)
+        st[(m0 >> 7) * C + c0 + c] = sc;
+}
+
+// ---------------------------------------------------------------------------
+// 128x128 weight blocks.  One CTA per block: 16 lanes cover a 128-wide row,
+// 16 rows per pass, 8 passes; amax through warp shuffles and a shared-memory
+// combine of the 8 warps.  With `qt` the codes are also staged in shared
+// memory and written transposed (each thread: 64 codes of one output row).
+// ---------------------------------------------------------------------------
+constexpr int Q3_THREADS = 256;
+
+__global__ void __launch_bounds__(Q3_THREADS)
+quantize_weight_kernel(const uint4 *__restrict__ w, int64_t N, int64_t K, uint2 *__restrict__ q,
+                       float *__restrict__ s, uint8_t *__restrict__ qt)
+{
+    __shared__ float s_red[Q3_THREADS / 32];
+    __shared__ __align__(16) uint8_t s_codes[128][128];
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const int sub = t & 15, r0 = t >> 4;
+    const int64_t bk = blockIdx.x, bn = blockIdx.y;
+    const int64_t K8 = K >> 3;
+
+    uint4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        v[i] = __ldcs(w + (bn * 128 + r0 + 16 * i) * K8 + bk * 16 + sub);
+
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        float f[8];
+        unpack8(v[i], f);
+        amax = fmaxf(amax, absmax8(f));
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1)
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if (lane == 0)
+        s_red[warp] = amax;
+    __syncthreads();
+    amax = s_red[0];
+#pragma unroll
+    for (int i = 1; i < Q3_THREADS / 32; ++i)
+        amax = fmaxf(amax, s_red[i]);
+    const float sc = amax / 448.0f;
+    if (t == 0)
+        s[bn * (K >> 7) + bk] = sc;
+
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        float f[8];
+        unpack8(v[i], f);
+        const uint2 codes = encode8(f, sc);
+        const int r = r0 + 16 * i;
+        __stcs(q + (bn * 128 + r) * K8 + bk * 16 + sub, codes);
+        if (qt != nullptr)
+            *reinterpret_cast<uint2 *>(&s_codes[r][sub * 8]) = codes;
+    }
+    if (qt == nullptr)
+        return;
+    __syncthreads();
+    // transposed write: output row kk (a column of the block), 64 codes
+    const int kk = t >> 1, hn = t & 1;
+    uint32_t o[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const int n = 64 * hn + 4 * i;
+        o[i] = static_cast<uint32_t>(s_codes[n][kk]) | (static_cast<uint32_t>(s_codes[n + 1][kk]) << 8) |
+               (static_cast<uint32_t>(s_codes[n + 2][kk]) << 16) |
+               (static_cast<uint32_t>(s_codes[n + 3][kk]) << 24);
+    }
+    uint4 *dst = reinterpret_cast<uint4 *>(qt + (bk * 128 + kk) * N + bn * 128 + 64 * hn);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        __stcs(dst + i, make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]));
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_act(const void *x, int64_t M, int64_t K, uint8_t *q, float *s, cudaStream_t stream)
+{
+    const int64_t G = K / 128;
+    dim3 grid(static_cast<unsigned>((M + Q1_ROWS - 1) / Q1_ROWS),
+              static_cast<unsigned>((G + Q1_GROUPS - 1) / Q1_GROUPS));
+    quantize_act_kernel<<<grid, Q1_THREADS, 0, stream>>>(static_cast<const uint4 *>(x), M, K,
+                                                         reinterpret_cast<uint2 *>(q), s);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_act_transposed(const void *x, int64_t M, int64_t C, uint8_t *qt, float *st,
+                                           cudaStream_t stream)
+{
+    dim3 grid(static_cast<unsigned>(M / Q2_ROWS), static_cast<unsigned>(C / Q2_COLS));
+    quantize_act_t_kernel<<<grid, Q2_THREADS, 0, stream>>>(static_cast<const uint4 *>(x), M, C, qt, st);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_weight(const void *w, int64_t N, int64_t K, uint8_t *q, float *s, uint8_t *qt,
+                                   cudaStream_t stream)
+{
+    dim3 grid(static_cast<unsigned>(K / 128), static_cast<unsigned>(N / 128));
+    quantize_weight_kernel<<<grid, Q3_THREADS, 0, stream>>>(static_cast<const uint4 *>(w), N, K,
+                                                            reinterpret_cast<uint2 *>(q), s, qt);
+    return cudaGetLastError();
+}
+
+}  // namespace jetfp8

@@ -288,3 +288,27 @@ def gemm_wgrad(qdyt, sdyt, qxt, sxt, rows=None, cols=None, threads: int = 1):
     N, M = qdyt.shape
     K = qxt.shape[0]
     return _gemm("jo_gemm_wgrad", qdyt, sdyt, qxt, sxt, M, N, K, (N, K), rows, cols, threads)
+
+
+# ------------------------------------------------------------ tolerance
+def bf16_ulp(ref: np.ndarray) -> np.ndarray:
+    """Spacing of bf16 numbers at |ref| (8 significant bits); below the
+    smallest normal (2^-126) the subnormal spacing 2^-133."""
+    a = np.abs(np.asarray(ref, dtype=np.float64))
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    ulp = np.exp2(e - 7)
+    return np.where(a >= 2.0 ** -126, ulp, 2.0 ** -133)
+
+
+def gemm_within_tolerance(got, ref, abssum, rel: float = 1e-3):
+    """The GEMM bar: |got - ref| <= rel * sum|a*b| + ulp_bf16(ref), per element.
+    Returns (all_ok, worst ratio err/bound, flat index of the worst)."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    bound = rel * np.asarray(abssum, dtype=np.float64) + bf16_ulp(ref)
+    ratio = np.abs(got - ref) / bound
+    if ratio.size == 0:
+        return True, 0.0, -1
+    worst = int(np.nanargmax(np.where(np.isnan(ratio), np.inf, ratio)))
+    ok = bool(np.all(np.isfinite(got)) and np.all(ratio <= 1.0))
+    return ok, float(ratio.ravel()[worst]), worst

@@ -1,0 +1,153 @@
+"""GPU quantisers vs the CPU oracle: codes and scales bit-exact.
+
+Covers tiny and ragged shapes (tails of every tile), special values (zero
+groups, bf16 subnormals, signed zeros, saturation, outlier channels), the
+8B-class layer shapes at full size, and the E4M3 convert itself over large
+slices of all fp32 bit patterns.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import e4m3_group_quantise_gb300 as jf
+from e4m3_group_quantise_gb300 import synthetic as syn
+from gpu_util import ORACLE_THREADS, assert_bitexact, bits, require_gpu
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    require_gpu()
+
+
+def special_values(M, K, seed):
+    """N(0,1) rows mixed with zero groups, subnormal groups, signed zeros,
+    large values and exact ties."""
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(M, K, generator=g)
+    x[0, :128] = 0.0                                    # zero group
+    if M > 1:
+        x[1, :128] = -0.0                               # negative-zero group
+        x[1, 5] = 3.0
+        x[1, 6] = -0.0
+    if M > 2:
+        x[2, :128] = torch.randn(128, generator=g) * 1e-39   # bf16 subnormals -> subnormal scale
+    if M > 3:
+        x[3, :128] = torch.randn(128, generator=g) * 3e38    # near the top of the range
+    if M > 4:
+        x[4, :128] = 448.0 * 2.0 ** -3                   # all equal to the amax
+    if M > 5 and K >= 256:
+        x[5, 128:256] = torch.tensor([2.125, 2.375, 1.9375, 56.0] * 32)  # ties after scaling
+    return x.to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("M,K", [(256, 512), (1, 128), (3, 384), (31, 1152), (33, 1024),
+                                 (64, 4096), (129, 256), (300, 2048), (1000, 128)])
+def test_quantize_act_bitexact(M, K):
+    x = syn.activation(M, K, seed=M * 7 + K, outlier_scale=20.0)
+    q, s = jf.quantize_act(x.to(DEV))
+    oq, os_ = oracle.quantize_act(bits(x))
+    assert_bitexact(q, oq, "codes")
+    assert_bitexact(s, os_, "scales")
+
+
+def test_quantize_act_special_values():
+    x = special_values(64, 512, 1)
+    q, s = jf.quantize_act(x.to(DEV))
+    oq, os_ = oracle.quantize_act(bits(x))
+    assert_bitexact(q, oq, "codes")
+    assert_bitexact(s, os_, "scales")
+    assert os_[0, 2] > 0 and os_[0, 2] < np.finfo(np.float32).tiny   # a subnormal scale was exercised
+
+
+@pytest.mark.parametrize("M,C", [(128, 128), (256, 512), (384, 640), (128, 4096), (1024, 384)])
+def test_quantize_act_transposed_bitexact(M, C):
+    x = syn.activation(M, C, seed=M + C, outlier_scale=20.0)
+    qt, st = jf.quantize_act_transposed(x.to(DEV))
+    oq, os_ = oracle.quantize_act_transposed(bits(x))
+    assert_bitexact(qt, oq, "codes")
+    assert_bitexact(st, os_, "scales")
+
+
+def test_quantize_act_transposed_special_values():
+    x = special_values(256, 256, 2).T.contiguous()     # groups along rows now hold the specials
+    qt, st = jf.quantize_act_transposed(x.to(DEV))
+    oq, os_ = oracle.quantize_act_transposed(bits(x))
+    assert_bitexact(qt, oq, "codes")
+    assert_bitexact(st, os_, "scales")
+
+
+@pytest.mark.parametrize("N,K", [(128, 128), (512, 512), (384, 1152), (6144, 4096)])
+@pytest.mark.parametrize("transposed", [True, False])
+def test_quantize_weight_bitexact(N, K, transposed):
+    w = syn.weight(N, K, seed=N + K)
+    q, s, qt = jf.quantize_weight(w.to(DEV), transposed=transposed)
+    oq, os_, oqt = oracle.quantize_weight(bits(w), transposed, threads=ORACLE_THREADS)
+    assert_bitexact(q, oq, "codes")
+    assert_bitexact(s, os_, "scales")
+    if transposed:
+        assert_bitexact(qt, oqt, "transposed codes")
+
+
+def test_quantize_weight_special_values():
+    w = special_values(256, 384, 3)
+    q, s, qt = jf.quantize_weight(w.to(DEV))
+    oq, os_, oqt = oracle.quantize_weight(bits(w), True)
+    assert_bitexact(q, oq, "codes")
+    assert_bitexact(s, os_, "scales")
+    assert_bitexact(qt, oqt, "transposed codes")
+
+
+def test_empty_inputs():
+    x = torch.empty(0, 256, dtype=torch.bfloat16, device=DEV)
+    q, s = jf.quantize_act(x)
+    assert q.shape == (0, 256) and s.shape == (2, 0)
+    qt, st = jf.quantize_act_transposed(x)
+    assert qt.shape == (256, 0)
+
+
+@pytest.mark.parametrize("name,shape", [("x_8b_hidden", (16384, 4096)), ("x_8b_inter", (16384, 14336))])
+def test_full_size_act_quantisers(name, shape):
+    """The 8B-class training-step activations at full size, every code compared."""
+    M, K = shape
+    x = syn.activation(M, K, seed=11, outlier_scale=20.0, device=DEV)
+    xb = bits(x)
+    q, s = jf.quantize_act(x)
+    oq, os_ = oracle.quantize_act(xb, threads=ORACLE_THREADS)
+    assert_bitexact(q, oq, "codes")
+    assert_bitexact(s, os_, "scales")
+    del q, s, oq, os_
+    qt, st = jf.quantize_act_transposed(x)
+    oqt, ost = oracle.quantize_act_transposed(xb, threads=ORACLE_THREADS)
+    assert_bitexact(qt, oqt, "transposed codes")
+    assert_bitexact(st, ost, "transposed scales")
+
+
+def test_full_size_gradient_slices():
+    """dY of the 8B gate_up projection [16384, 28672]: full-tensor quantisers on
+    the GPU, checked on column slices (the transposed quantiser's groups are
+    per column, so a slice is an exact sub-problem) and full row-blocks."""
+    M, N = 16384, 28672
+    dy = syn.grad_output(M, N, seed=5, device=DEV)
+    q, s = jf.quantize_act(dy)
+    qt, st = jf.quantize_act_transposed(dy)
+    rows = slice(8192, 8192 + 512)
+    sub = bits(dy[rows])
+    oq, os_ = oracle.quantize_act(sub, threads=ORACLE_THREADS)
+    assert_bitexact(q[rows], oq, "codes (row block)")
+    assert_bitexact(s[:, rows].contiguous(), os_, "scales (row block)")
+    for c0 in (0, 12800, N - 128):
+        sl = slice(c0, c0 + 128)
+        oqt, ost = oracle.quantize_act_transposed(bits(dy[:, sl]), threads=ORACLE_THREADS)
+        assert_bitexact(qt[sl], oqt, f"transposed codes cols {c0}")
+        assert_bitexact(st[:, sl].contiguous(), ost, f"transposed scales cols {c0}")
+
+
+def test_repeatable():
+    x = syn.activation(512, 2048, seed=3, device=DEV)
+    a = jf.quantize_act(x)
+    b = jf.quantize_act(x)
+    assert all(torch.equal(u, v) for u, v in zip(a, b))

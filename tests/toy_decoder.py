@@ -1,0 +1,59 @@
+"""A 2-layer toy decoder whose every linear layer (LM head included) runs the
+FP8 path -- test fixture for the unified rollout/training precision flow.
+
+Per layer: RMSNorm -> QKV -> causal softmax attention (4 heads x 128, fp32
+softmax, no positional encoding) -> O -> residual -> RMSNorm -> gate_up
+(2 x 1536) -> SiLU(gate) * up -> down -> residual.  Then a final RMSNorm and
+the LM head [vocab 4096, hidden 512].  Weights ~ N(0, 0.02), seed 0.
+The non-linear ops use plain PyTorch (they are not on the FP8 GEMM path).
+"""
+import torch
+
+from e4m3_group_quantise_gb300 import FP8Linear
+
+HIDDEN, HEADS, HEAD_DIM, INTER, VOCAB, LAYERS = 512, 4, 128, 1536, 4096, 2
+
+
+def rmsnorm(x, w, eps=1e-6):
+    xf = x.float()
+    return (xf * torch.rsqrt(xf.pow(2).mean(-1, keepdim=True) + eps) * w.float()).to(torch.bfloat16)
+
+
+class ToyDecoder(torch.nn.Module):
+    def __init__(self, device="cuda", seed=0):
+        super().__init__()
+        g = torch.Generator(device="cpu").manual_seed(seed)
+        self.embed = torch.nn.Parameter((torch.randn(VOCAB, HIDDEN, generator=g) * 0.02).to(torch.bfloat16).to(device))
+        self.layers = torch.nn.ModuleList()
+        for _ in range(LAYERS):
+            lyr = torch.nn.Module()
+            lyr.qkv = FP8Linear(HIDDEN, 3 * HEADS * HEAD_DIM, device=device)
+            lyr.o = FP8Linear(HEADS * HEAD_DIM, HIDDEN, device=device)
+            lyr.gate_up = FP8Linear(HIDDEN, 2 * INTER, device=device)
+            lyr.down = FP8Linear(INTER, HIDDEN, device=device)
+            lyr.n1 = torch.nn.Parameter(torch.ones(HIDDEN, dtype=torch.bfloat16, device=device))
+            lyr.n2 = torch.nn.Parameter(torch.ones(HIDDEN, dtype=torch.bfloat16, device=device))
+            self.layers.append(lyr)
+        self.norm = torch.nn.Parameter(torch.ones(HIDDEN, dtype=torch.bfloat16, device=device))
+        self.head = FP8Linear(HIDDEN, VOCAB, device=device)
+        with torch.no_grad():
+            for m in self.modules():
+                if isinstance(m, FP8Linear):
+                    m.weight.copy_((torch.randn(m.weight.shape, generator=g) * 0.02).to(torch.bfloat16))
+
+    def forward(self, tokens):
+        B, T = tokens.shape
+        h = self.embed[tokens]                                  # [B, T, H] bf16
+        mask = torch.ones(T, T, dtype=torch.bool, device=tokens.device).tril()
+        for lyr in self.layers:
+            a = lyr.qkv(rmsnorm(h, lyr.n1))                     # [B, T, 3*H]
+            q, k, v = a.float().view(B, T, 3, HEADS, HEAD_DIM).unbind(2)
+            q, k, v = (t.transpose(1, 2) for t in (q, k, v))     # [B, heads, T, d]
+            att = (q @ k.transpose(-1, -2)) / HEAD_DIM ** 0.5
+            att = att.masked_fill(~mask, float("-inf")).softmax(-1)
+            ctx = (att @ v).transpose(1, 2).reshape(B, T, HEADS * HEAD_DIM).to(torch.bfloat16)
+            h = h + lyr.o(ctx)
+            gu = lyr.gate_up(rmsnorm(h, lyr.n2)).float()
+            gate, up = gu.chunk(2, dim=-1)
+            h = h + lyr.down((torch.nn.functional.silu(gate) * up).to(torch.bfloat16))
+        return self.head(rmsnorm(h, self.norm))                 # logits [B, T, V] bf16

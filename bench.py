@@ -1,0 +1,415 @@
+"""Benchmark: one FP8 linear-layer training step over the four projections of
+an 8B-class decoder layer at 16384 tokens.
+
+A step runs every stage of the path for each projection (QKV 6144x4096,
+O 4096x4096, gate_up 28672x4096, down 4096x14336; M = 16384 tokens = 8 x 2048):
+  quantise W (128x128 blocks, + transposed codes), quantise X (1x128) and
+  X^T (128x1), quantise dY (1x128) and dY^T (128x1), then Fprop, Dgrad, Wgrad.
+Metric: block-scaled FP8 GEMM TFLOP/s = (Fprop + Dgrad + Wgrad FLOPs, 2MNK
+each) / step time, the step time including the quantisers.  Inputs are
+synthetic (seeded) and resident in HBM; the step's working set (~8 GB) is far
+larger than L2, so no explicit flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (the plain C restatement of the
+method) on a bounded sample of the same workload on the host cores.
+Under torchrun (N > 1) every rank runs the same step on its own GPU over its
+own tokens (weak scaling, no collective on the data path); the time is the
+maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "block-scaled FP8 GEMM TFLOP/s (fprop/dgrad/wgrad), % of GB300 FP8 peak"
+TOKENS = 16384
+PROJ = {"qkv": (6144, 4096), "o": (4096, 4096), "gate_up": (28672, 4096), "down": (4096, 14336)}
+WORKLOAD = ("train-8b: full FP8 training step (quantise W, X, X^T, dY, dY^T; fprop, dgrad, wgrad) on the "
+            "four 8B-class projections qkv 6144x4096, o 4096x4096, gate_up 28672x4096, down 4096x14336 "
+            "at M=16384 tokens (8 x 2048)")
+FP8_PER_BF16 = 4.5 / 2.25          # nominal dense fp8 : bf16 tensor ratio
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNELS = ("quant_w", "quant_x", "quant_xt", "quant_dy", "quant_dyt", "fprop", "dgrad", "wgrad")
+
+
+def gemm_flops() -> float:
+    return sum(3 * 2.0 * TOKENS * n * k for n, k in PROJ.values())
+
+
+def quant_bytes(kind: str, n: int, k: int) -> float:
+    """Algorithmic bytes of one quantiser launch."""
+    if kind == "quant_w":                      # read bf16, write codes + transposed codes + scales
+        return n * k * (2 + 1 + 1) + 4 * (n // 128) * (k // 128)
+    rows, cols = {"quant_x": (TOKENS, k), "quant_xt": (TOKENS, k),
+                  "quant_dy": (TOKENS, n), "quant_dyt": (TOKENS, n)}[kind]
+    return rows * cols * (2 + 1 + 4 / 128)
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return FALLBACK, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = []
+        for line in self.out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, flags in rows for i, f in enumerate(flags) if f == "Active"})
+        return {"sm_mhz": float(np.median([r[0] for r in rows])), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ our arm
+class Step:
+    """Buffers and launches of one training step (all four projections)."""
+
+    def __init__(self, device, seed: int):
+        import e4m3_group_quantise_gb300 as jf
+        from e4m3_group_quantise_gb300 import synthetic as syn
+        self.jf = jf
+        self.p = {}
+        for i, (name, (n, k)) in enumerate(PROJ.items()):
+            d = {}
+            d["x"] = syn.activation(TOKENS, k, seed=seed, index=i, device=device, outlier_scale=20.0)
+            d["w"] = syn.weight(n, k, seed=seed, index=i, device=device)
+            d["dy"] = syn.grad_output(TOKENS, n, seed=seed, index=i, device=device)
+            e = lambda *s, dt=torch.uint8: torch.empty(*s, dtype=dt, device=device)  # noqa: E731
+            f32 = torch.float32
+            d["qw"], d["sw"], d["qwt"] = e(n, k), e(n // 128, k // 128, dt=f32), e(k, n)
+            d["qx"], d["sx"] = e(TOKENS, k), e(k // 128, TOKENS, dt=f32)
+            d["qxt"], d["sxt"] = e(k, TOKENS), e(TOKENS // 128, k, dt=f32)
+            d["qdy"], d["sdy"] = e(TOKENS, n), e(n // 128, TOKENS, dt=f32)
+            d["qdyt"], d["sdyt"] = e(n, TOKENS), e(TOKENS // 128, n, dt=f32)
+            d["y"] = e(TOKENS, n, dt=torch.bfloat16)
+            d["dx"] = e(TOKENS, k, dt=torch.bfloat16)
+            d["dw"] = e(n, k, dt=torch.bfloat16)
+            self.p[name] = d
+
+    def launches(self, d):
+        jf = self.jf
+        return (
+            ("quant_w", lambda: jf.jetfp8_quantize_weight(d["w"], d["qw"], d["sw"], d["qwt"])),
+            ("quant_x", lambda: jf.jetfp8_quantize_act(d["x"], d["qx"], d["sx"])),
+            ("quant_xt", lambda: jf.jetfp8_quantize_act_transposed(d["x"], d["qxt"], d["sxt"])),
+            ("quant_dy", lambda: jf.jetfp8_quantize_act(d["dy"], d["qdy"], d["sdy"])),
+            ("quant_dyt", lambda: jf.jetfp8_quantize_act_transposed(d["dy"], d["qdyt"], d["sdyt"])),
+            ("fprop", lambda: jf.jetfp8_gemm_fprop(d["qx"], d["sx"], d["qw"], d["sw"], d["y"])),
+            ("dgrad", lambda: jf.jetfp8_gemm_dgrad(d["qdy"], d["sdy"], d["qwt"], d["sw"], d["dx"])),
+            ("wgrad", lambda: jf.jetfp8_gemm_wgrad(d["qdyt"], d["sdyt"], d["qxt"], d["sxt"], d["dw"])),
+        )
+
+    def run(self, events=None):
+        """Enqueue one step; with `events`, record one event after each launch."""
+        for name, d in self.p.items():
+            for kind, fn in self.launches(d):
+                fn()
+                if events is not None:
+                    ev = torch.cuda.Event(enable_timing=True)
+                    ev.record()
+                    events.append((name, kind, ev))
+
+
+def time_ours(args, rank, world, device):
+    step = Step(device, seed=1000 + rank)
+    for _ in range(args.warmup):
+        step.run()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+
+    start = torch.cuda.Event(enable_timing=True)
+    events = []
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        start.record()
+        for _ in range(args.steps):
+            step.run(events)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    total_ms = start.elapsed_time(events[-1][2])
+
+    # per-kernel durations from consecutive events (same stream, back to back)
+    per = {}
+    prev = start
+    for name, kind, ev in events:
+        per.setdefault(kind, []).append((name, prev.elapsed_time(ev)))
+        prev = ev
+    return step, total_ms, per, clk.summary()
+
+
+def time_e2e(step, steps, device):
+    """Same step through the public API with host buffers: each step copies
+    the inputs from pinned host memory and the results back."""
+    host = {}
+    h2d = d2h = 0
+    for name, d in step.p.items():
+        h = {}
+        for key in ("x", "w", "dy"):
+            h[key] = torch.empty(d[key].shape, dtype=d[key].dtype, pin_memory=True)
+            h[key].copy_(d[key])
+            h2d += d[key].numel() * d[key].element_size()
+        for key in ("y", "dx", "dw"):
+            h[key] = torch.empty(d[key].shape, dtype=d[key].dtype, pin_memory=True)
+            d2h += d[key].numel() * d[key].element_size()
+        host[name] = h
+
+    def one():
+        for name, d in step.p.items():
+            h = host[name]
+            for key in ("x", "w", "dy"):
+                d[key].copy_(h[key], non_blocking=True)
+            for _, fn in step.launches(d):
+                fn()
+            for key in ("y", "dx", "dw"):
+                h[key].copy_(d[key], non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        one()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    return ms, h2d, d2h
+
+
+def cpu_oracle_sample(seed: int = 7):
+    """The oracle on a bounded sample of the O projection (N = K = 4096,
+    M = 16384): quantise what the sample needs, then Fprop on 4 token rows,
+    Dgrad on 4 token rows, Wgrad on 1 output row over all 16384 tokens.
+    Returns (seconds, GEMM flops, description)."""
+    import oracle
+    from e4m3_group_quantise_gb300 import synthetic as syn
+    n, k = PROJ["o"]
+    x = syn.activation(TOKENS, k, seed=seed, outlier_scale=20.0)
+    w = syn.weight(n, k, seed=seed)
+    dy = syn.grad_output(TOKENS, n, seed=seed)
+    xb, wb, dyb = syn.bf16_bits(x), syn.bf16_bits(w), syn.bf16_bits(dy)
+    t0 = time.perf_counter()
+    qx, sx = oracle.quantize_act(xb[:4])
+    qw, sw, _ = oracle.quantize_weight(wb)
+    qdy, sdy = oracle.quantize_act(dyb[:4])
+    qxt, sxt = oracle.quantize_act_transposed(xb)
+    qdyt, sdyt = oracle.quantize_act_transposed(np.ascontiguousarray(dyb[:, :128]))
+    r = np.repeat(np.arange(4), n)
+    c = np.tile(np.arange(n), 4)
+    oracle.gemm_fprop(qx, sx, qw, sw, r, c)
+    r = np.repeat(np.arange(4), k)
+    c = np.tile(np.arange(k), 4)
+    oracle.gemm_dgrad(qdy, sdy, qw, sw, r, c)
+    oracle.gemm_wgrad(qdyt, sdyt, qxt, sxt, np.zeros(k, np.int64), np.arange(k, dtype=np.int64))
+    secs = time.perf_counter() - t0
+    flops = 2.0 * (4 * n * k + 4 * k * n + 1 * k * TOKENS)
+    desc = ("oracle (plain C, 1 thread) on the o projection 4096x4096 at M=16384: quantise the needed "
+            "inputs, fprop 4 token rows, dgrad 4 token rows, wgrad 1 output row over 16384 tokens")
+    return secs, flops, desc
+
+
+# ------------------------------------------------------------------ main
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import datetime
+        torch.distributed.init_process_group("nccl" if args.impl == "ours" else "gloo",
+                                             timeout=datetime.timedelta(minutes=10))
+    return rank, world, local
+
+
+def max_over_ranks(value: float, world: int, device) -> float:
+    if world == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    rank, world, local = dist_setup(args)
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    import __graft_entry__
+    __graft_entry__.build()
+
+    step, total_ms, per, clocks = time_ours(args, rank, world, device)
+    ms_step = max_over_ranks(total_ms / args.steps, world, device)
+    flops = gemm_flops()
+    value = world * flops / (ms_step * 1e-3) / 1e12
+
+    pk, src = peaks()
+    fp8_sustained = pk["bf16_tflops_sustained"] * FP8_PER_BF16
+    kernels = {}
+    for kind, rows in per.items():
+        ms = sum(t for _, t in rows) / args.steps
+        entry = {"ms_per_step": round(ms, 4), "launches_per_step": len(rows) // args.steps}
+        if kind in ("fprop", "dgrad", "wgrad"):
+            entry["tflops"] = round(sum(2.0 * TOKENS * n * k for n, k in PROJ.values()) / (ms * 1e-3) / 1e12, 1)
+        else:
+            byts = sum(quant_bytes(kind, n, k) for n, k in PROJ.values())
+            entry["gbs"] = round(byts / (ms * 1e-3) / 1e9, 1)
+            entry["frac_of_hbm"] = round(entry["gbs"] / pk["hbm_gbs"], 3)
+        kernels[kind] = entry
+    gemm_ms = sum(kernels[k]["ms_per_step"] for k in ("fprop", "dgrad", "wgrad"))
+    gemm_achieved = flops / (gemm_ms * 1e-3) / 1e12
+    launches = sum(len(r) for r in per.values())
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+        "data": "synthetic (seeded; X N(0,1) with 1% channels x20, W N(0,0.02), dY N(0,1e-2))",
+        "config": {"workload": WORKLOAD, "tokens_per_gpu": TOKENS,
+                   "projections": {k: list(v) for k, v in PROJ.items()},
+                   "l2": "inputs larger than L2 (per-step working set ~8 GB vs 129 MB L2); no flush"},
+        "pct_of_fp8_peak": round(100.0 * value / world / fp8_sustained, 1),
+        "roofline": {"kernel": "gemm (fprop+dgrad+wgrad launches)", "bound": "tensor",
+                     "achieved": round(gemm_achieved, 1), "peak": round(fp8_sustained, 1), "unit": "TFLOP/s",
+                     "frac": round(gemm_achieved / fp8_sustained, 3), "traffic": None,
+                     "peak_note": f"{src} bf16_tflops_sustained x {FP8_PER_BF16} (nominal fp8:bf16 ratio), "
+                                  f"'of {src}'"},
+        "kernels": kernels,
+        "gpu_launches": launches,
+        "clocks": clocks,
+    }
+    if not args.no_e2e:
+        e_ms, h2d, d2h = time_e2e(step, max(3, min(args.steps // 10, 10)), device)
+        e_ms = max_over_ranks(e_ms, world, device)
+        result["e2e"] = {"value": round(world * flops / (e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                         "ms_per_step": round(e_ms, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        secs, cflops, desc = cpu_oracle_sample()
+        result["cpu_baseline"] = {"value": cflops / secs / 1e12, "unit": "TFLOP/s", "cores": 1,
+                                  "kind": "oracle", "sample": desc, "seconds": round(secs, 2)}
+    if rank == 0:
+        print(json.dumps(result))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return result
+
+
+def run_reference(args, rank, world):
+    """The oracle as it stands, timed on the host cores: each step is the
+    bounded sample of `cpu_oracle_sample` scaled down to one token row."""
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return None
+    import oracle
+    from e4m3_group_quantise_gb300 import synthetic as syn
+    oracle.build()
+    n, k = PROJ["o"]
+    x = syn.activation(TOKENS, k, seed=7, outlier_scale=20.0)
+    w = syn.weight(n, k, seed=7)
+    dy = syn.grad_output(TOKENS, n, seed=7)
+    xb, wb, dyb = syn.bf16_bits(x), syn.bf16_bits(w), syn.bf16_bits(dy)
+
+    def one():
+        qx, sx = oracle.quantize_act(xb[:1])
+        qw, sw, _ = oracle.quantize_weight(wb[:128])
+        qdy, sdy = oracle.quantize_act(np.ascontiguousarray(dyb[:1, :128]))   # contraction over one N group
+        qxt, sxt = oracle.quantize_act_transposed(np.ascontiguousarray(xb[:, :1024]))
+        qdyt, sdyt = oracle.quantize_act_transposed(np.ascontiguousarray(dyb[:, :128]))
+        cols = np.arange(128, dtype=np.int64)
+        oracle.gemm_fprop(qx, sx, qw, sw, np.zeros(128, np.int64), cols)
+        oracle.gemm_dgrad(qdy, sdy, qw, sw, np.zeros(128, np.int64), cols)
+        oracle.gemm_wgrad(qdyt, sdyt, qxt, sxt, np.zeros(1024, np.int64), np.arange(1024, dtype=np.int64))
+        return 2.0 * (128 * k + 128 * 128 + 1024 * TOKENS)
+
+    for _ in range(args.warmup):
+        one()
+    t0 = time.perf_counter()
+    flops = sum(one() for _ in range(args.steps))
+    secs = time.perf_counter() - t0
+    value = flops / secs / 1e12
+    sample = ("oracle (plain C, 1 thread) per step: quantise 1 token row of X, 128 values of dY, one "
+              "128-row weight band, 1024 columns of X^T and 128 of dY^T; fprop 128 outputs of one token "
+              "row (K=4096), dgrad 128 outputs over one 128-wide N group, wgrad 1024 outputs of one dW "
+              "row over 16384 tokens (o projection, M=16384)")
+    res = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic", "config": {"workload": WORKLOAD, "tokens_per_gpu": TOKENS},
+           "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "sample": sample},
+           "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(res))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return res
+
+
+if __name__ == "__main__":
+    main()

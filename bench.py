@@ -292,9 +292,14 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
+    ap.add_argument("--case", default=None,
+                    help="time one kernel alone, e.g. fprop:16384x6144x4096 (KIND:MxNxK; KIND in fprop, dgrad, "
+                         "wgrad, quant_x, quant_xt, quant_w) -- a single-kernel line for profiling, not the metric")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.case:
+        return run_case(args)
 
     rank, world, local = dist_setup(args)
     if args.impl == "reference":
@@ -359,6 +364,69 @@ def main(argv=None):
     if world > 1:
         torch.distributed.destroy_process_group()
     return result
+
+
+def run_case(args):
+    """One kernel on one shape: warm-up, then `steps` launches timed with CUDA
+    events on the launching stream (inputs larger than L2 for the big shapes)."""
+    import __graft_entry__
+    __graft_entry__.build()
+    import e4m3_group_quantise_gb300 as jf
+    from e4m3_group_quantise_gb300 import synthetic as syn
+    kind, dims = args.case.split(":")
+    M, N, K = (int(v) for v in dims.lower().split("x"))
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    if kind == "fprop":
+        qx, sx = jf.quantize_act(syn.activation(M, K, seed=1, device=dev, outlier_scale=20.0))
+        qw, sw, _ = jf.quantize_weight(syn.weight(N, K, seed=1, device=dev), transposed=False)
+        out = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        fn = lambda: jf.jetfp8_gemm_fprop(qx, sx, qw, sw, out)  # noqa: E731
+    elif kind == "dgrad":
+        qdy, sdy = jf.quantize_act(syn.grad_output(M, N, seed=1, device=dev))
+        qw, sw, qwt = jf.quantize_weight(syn.weight(N, K, seed=1, device=dev))
+        out = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
+        fn = lambda: jf.jetfp8_gemm_dgrad(qdy, sdy, qwt, sw, out)  # noqa: E731
+    elif kind == "wgrad":
+        qxt, sxt = jf.quantize_act_transposed(syn.activation(M, K, seed=1, device=dev, outlier_scale=20.0))
+        qdyt, sdyt = jf.quantize_act_transposed(syn.grad_output(M, N, seed=1, device=dev))
+        out = torch.empty(N, K, dtype=torch.bfloat16, device=dev)
+        fn = lambda: jf.jetfp8_gemm_wgrad(qdyt, sdyt, qxt, sxt, out)  # noqa: E731
+    elif kind in ("quant_x", "quant_xt"):
+        x = syn.activation(M, K, seed=1, device=dev, outlier_scale=20.0)
+        if kind == "quant_x":
+            q, s = torch.empty(M, K, dtype=torch.uint8, device=dev), torch.empty(K // 128, M, device=dev)
+            fn = lambda: jf.jetfp8_quantize_act(x, q, s)  # noqa: E731
+        else:
+            q, s = torch.empty(K, M, dtype=torch.uint8, device=dev), torch.empty(M // 128, K, device=dev)
+            fn = lambda: jf.jetfp8_quantize_act_transposed(x, q, s)  # noqa: E731
+    elif kind == "quant_w":
+        w = syn.weight(N, K, seed=1, device=dev)
+        q, s = torch.empty(N, K, dtype=torch.uint8, device=dev), torch.empty(N // 128, K // 128, device=dev)
+        qt = torch.empty(K, N, dtype=torch.uint8, device=dev)
+        fn = lambda: jf.jetfp8_quantize_weight(w, q, s, qt)  # noqa: E731
+    else:
+        raise SystemExit(f"unknown case kind {kind}")
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    evs[0].record()
+    for i in range(args.steps):
+        fn()
+        evs[i + 1].record()
+    torch.cuda.synchronize()
+    times = [evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps)]
+    ms = float(np.median(times))
+    rec = {"case": args.case, "ms_median": round(ms, 5), "ms_min": round(min(times), 5), "launches": args.steps}
+    if kind in ("fprop", "dgrad", "wgrad"):
+        rec["tflops"] = round(2.0 * M * N * K / (ms * 1e-3) / 1e12, 1)
+    else:
+        byts = N * K * 4 + 4 * (N // 128) * (K // 128) if kind == "quant_w" else M * K * (3 + 4 / 128)
+        rec["gbs"] = round(byts / (ms * 1e-3) / 1e9, 1)
+    assert jf.jetfp8_poll_device_error() == 0
+    print(json.dumps(rec))
+    return rec
 
 
 def run_reference(args, rank, world):

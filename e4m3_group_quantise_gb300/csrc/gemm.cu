@@ -74,10 +74,13 @@ struct Smem {
     static constexpr uint32_t B_BYTES = BN * BK;
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr uint32_t TILES = STAGES * STAGE_BYTES;
-    static constexpr uint32_t BAR_OFF = TILES;
+    // per-column B scales, double-buffered per promotion warp: [8 warps][2][BN/2] fp32
+    static constexpr uint32_t SB_OFF = TILES;
+    static constexpr uint32_t SB_BYTES = 8 * 2 * (BN / 2) * 4;
+    static constexpr uint32_t BAR_OFF = SB_OFF + SB_BYTES;
     // full[S], empty[S], tfull[2], tempty[2], mma_done, tmem holder, abort flag
     static constexpr uint32_t CTRL_BYTES = (2 * STAGES + 5) * 8 + 16;
-    static constexpr uint32_t TOTAL = 1024 /* alignment slack */ + TILES + CTRL_BYTES;
+    static constexpr uint32_t TOTAL = 1024 /* alignment slack */ + BAR_OFF + CTRL_BYTES;
 };
 
 __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int &tm, int &tn)
@@ -235,6 +238,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         const int wg = (warp - FIRST_PROMO_WARP) >> 2;   // 0 or 1: column half of the tile
         const int quarter = warp & 3;         // TMEM lanes 32*quarter .. +31
         const int row_in_tile = quarter * 32 + lane;
+        float *my_sb = reinterpret_cast<float *>(smem + L::SB_OFF) + (warp - FIRST_PROMO_WARP) * 2 * COLS_PER_WG;
         uint32_t it = 0;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
@@ -249,6 +253,19 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
             for (int i = 0; i < COLS_PER_WG; ++i)
                 acc[i] = 0.0f;
 
+            // Per-column scales (Wgrad): each warp copies its 128 (or 64) scales of
+            // group g+1 into its own smem buffer while it promotes group g.
+            auto prefetch_sb = [&](int g) {
+                if (SB_PER_COLUMN) {
+                    __syncwarp();
+                    constexpr int CHUNKS16 = COLS_PER_WG / 4;   // 16-byte pieces
+                    if (cols_ok && lane < CHUNKS16)
+                        ptx::cp_async_16(my_sb + (g & 1) * COLS_PER_WG + 4 * lane,
+                                         args.sb + static_cast<int64_t>(g) * args.sb_stride_g + col0 + 4 * lane);
+                    ptx::cp_async_commit();
+                }
+            };
+            prefetch_sb(0);
             float sa_next = row_ok ? __ldg(args.sa + row) : 0.0f;
             for (int g = 0; g < G; ++g, ++it) {
                 const uint32_t buf = it & 1u;
@@ -257,9 +274,18 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                 if (g + 1 < G)
                     sa_next = row_ok ? __ldg(args.sa + static_cast<int64_t>(g + 1) * args.rows + row) : 0.0f;
                 float w_blk = 0.0f;
-                const float *sbg = args.sb + static_cast<int64_t>(g) * args.sb_stride_g;
-                if (!SB_PER_COLUMN)
+                if (!SB_PER_COLUMN) {
+                    const float *sbg = args.sb + static_cast<int64_t>(g) * args.sb_stride_g;
                     w_blk = sa * (cols_ok ? __ldg(sbg + static_cast<int64_t>(col0 >> 7) * args.sb_stride_c) : 0.0f);
+                } else {
+                    if (g + 1 < G)
+                        prefetch_sb(g + 1);
+                    else
+                        ptx::cp_async_commit();          // keep one group in flight for the wait below
+                    ptx::cp_async_wait<1>();             // group g's scales have landed
+                    __syncwarp();
+                }
+                const float *sb_cur = my_sb + (g & 1) * COLS_PER_WG;
 
                 if (!ptx::mbar_wait(&tfull[buf], bphase, abort_flag, args.err, ERRBIT_PROMOTE, WAIT_TIMEOUT_NS)) {
                     ok = false;
@@ -284,10 +310,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                             ptx::mbar_arrive(&tempty[buf]);
                     }
                     if (SB_PER_COLUMN) {
-                        const float4 *sbv = reinterpret_cast<const float4 *>(sbg + col0 + c * 32);
+                        const float4 *sbv = reinterpret_cast<const float4 *>(sb_cur + c * 32);
 #pragma unroll
                         for (int v = 0; v < 8; ++v) {
-                            const float4 s4 = cols_ok ? __ldg(sbv + v) : make_float4(0.f, 0.f, 0.f, 0.f);
+                            const float4 s4 = sbv[v];
                             acc[c * 32 + 4 * v + 0] = fmaf(__uint_as_float(cur[4 * v + 0]), sa * s4.x, acc[c * 32 + 4 * v + 0]);
                             acc[c * 32 + 4 * v + 1] = fmaf(__uint_as_float(cur[4 * v + 1]), sa * s4.y, acc[c * 32 + 4 * v + 1]);
                             acc[c * 32 + 4 * v + 2] = fmaf(__uint_as_float(cur[4 * v + 2]), sa * s4.z, acc[c * 32 + 4 * v + 2]);

@@ -23,6 +23,8 @@
 //   warp 0, lane 0 : TMA producer   -- A and B tiles of one group per smem stage
 //   warp 1, lane 0 : MMA issuer     -- 4 x tcgen05.mma (K = 32 each) per group
 //                                      into one of two TMEM partial buffers
+//   warp 2         : scale loader   -- cp.async of the group's row scales (128)
+//                                      and column scales into a smem ring
 //   warps 4..11    : promotion      -- two warpgroups, each 128 rows x BN/2
 //                                      columns; tcgen05.ld the partial, free the
 //                                      buffer, acc += partial * sa * sb; bf16
@@ -50,7 +52,9 @@ constexpr int BK = 128;                  // one scale group
 constexpr int NUM_THREADS = 384;
 constexpr int PRODUCER_WARP = 0;
 constexpr int MMA_WARP = 1;
+constexpr int SCALE_WARP = 2;
 constexpr int FIRST_PROMO_WARP = 4;
+constexpr int SCALE_STAGES = 4;
 constexpr uint32_t CTRL_REGS = 40;
 constexpr uint32_t PROMO_REGS = 232;
 static_assert(128 * CTRL_REGS + 256 * PROMO_REGS <= NUM_THREADS * 168, "register split exceeds the launch allocation");
@@ -74,12 +78,13 @@ struct Smem {
     static constexpr uint32_t B_BYTES = BN * BK;
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr uint32_t TILES = STAGES * STAGE_BYTES;
-    // per-column B scales, double-buffered per promotion warp: [8 warps][2][BN/2] fp32
-    static constexpr uint32_t SB_OFF = TILES;
-    static constexpr uint32_t SB_BYTES = 8 * 2 * (BN / 2) * 4;
-    static constexpr uint32_t BAR_OFF = SB_OFF + SB_BYTES;
-    // full[S], empty[S], tfull[2], tempty[2], mma_done, tmem holder, abort flag
-    static constexpr uint32_t CTRL_BYTES = (2 * STAGES + 5) * 8 + 16;
+    // scale ring: per slot 128 row scales then BN column scales (fp32)
+    static constexpr uint32_t SCALE_FLOATS = BM + BN;
+    static constexpr uint32_t SCALE_OFF = TILES;
+    static constexpr uint32_t SCALE_BYTES = SCALE_STAGES * SCALE_FLOATS * 4;
+    static constexpr uint32_t BAR_OFF = SCALE_OFF + SCALE_BYTES;
+    // full[S], empty[S], sfull[SS], sempty[SS], tfull[2], tempty[2], mma_done, tmem holder, abort flag
+    static constexpr uint32_t CTRL_BYTES = (2 * STAGES + 2 * SCALE_STAGES + 5) * 8 + 16;
     static constexpr uint32_t TOTAL = 1024 /* alignment slack */ + BAR_OFF + CTRL_BYTES;
 };
 
@@ -115,9 +120,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sA = smem;
     uint8_t *sB = smem + STAGES * L::A_BYTES;
+    float *scl = reinterpret_cast<float *>(smem + L::SCALE_OFF);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::BAR_OFF);
     uint64_t *empty = full + STAGES;
-    uint64_t *tfull = empty + STAGES;
+    uint64_t *sfull = empty + STAGES;
+    uint64_t *sempty = sfull + SCALE_STAGES;
+    uint64_t *tfull = sempty + SCALE_STAGES;
     uint64_t *tempty = tfull + 2;
     uint64_t *mma_done = tempty + 2;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(mma_done + 1);
@@ -134,9 +142,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                 ptx::mbar_init(&full[s], 1);
                 ptx::mbar_init(&empty[s], 1);
             }
+            for (int s = 0; s < SCALE_STAGES; ++s) {
+                ptx::mbar_init(&sfull[s], 32);   // every loader lane's copies
+                ptx::mbar_init(&sempty[s], 8);   // one arrival per promotion warp
+            }
             for (int b = 0; b < 2; ++b) {
                 ptx::mbar_init(&tfull[b], 1);
-                ptx::mbar_init(&tempty[b], 8);   // one arrival per promotion warp (8 warps)
+                ptx::mbar_init(&tempty[b], 8);   // one arrival per promotion warp
             }
             ptx::mbar_init(mma_done, 1);
             *abort_flag = 0;
@@ -154,138 +166,168 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     const uint32_t tmem_base = *tmem_holder;
 
     if (warp < FIRST_PROMO_WARP) {
-      ptx::setmaxnreg_dec<CTRL_REGS>();
-      if (warp == PRODUCER_WARP) {
-        // ------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
-            uint32_t issued_mask = 0, issued_parity = 0;
+        ptx::setmaxnreg_dec<CTRL_REGS>();
+        if (warp == PRODUCER_WARP) {
+            // -------------------------------------------------- TMA producer
+            if (lane == 0) {
+                int stage = 0;
+                uint32_t phase = 0;
+                uint32_t issued_mask = 0, issued_parity = 0;
+                bool ok = true;
+                for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+                    int tm, tn;
+                    tile_coords(tile, args.tiles_m, args.tiles_n, tm, tn);
+                    for (int g = 0; g < G; ++g) {
+                        if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, args.err, ERRBIT_PRODUCER,
+                                            WAIT_TIMEOUT_NS)) {
+                            ok = false;
+                            break;
+                        }
+                        ptx::mbar_arrive_expect_tx(&full[stage], L::STAGE_BYTES);
+                        ptx::tma_load_2d(sA + stage * L::A_BYTES, &tmap_a, &full[stage], g * BK, tm * BM);
+                        ptx::tma_load_2d(sB + stage * L::B_BYTES, &tmap_b, &full[stage], g * BK, tn * BN);
+                        issued_mask |= 1u << stage;
+                        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                        if (++stage == STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                }
+                if (!ok) {
+                    // drain: every copy this thread started must land before exit
+                    for (int s = 0; s < STAGES; ++s)
+                        if (issued_mask & (1u << s))
+                            ptx::mbar_wait(&full[s], (issued_parity >> s) & 1u, nullptr, args.err, ERRBIT_DRAIN,
+                                           WAIT_TIMEOUT_NS);
+                }
+            }
+            __syncwarp();
+        } else if (warp == MMA_WARP) {
+            // -------------------------------------------------- MMA issuer
+            if (lane == 0) {
+                int stage = 0;
+                uint32_t phase = 0;
+                uint32_t it = 0;   // global group counter -> TMEM buffer / phase
+                bool ok = true;
+                const uint32_t a_base = ptx::smem_u32(sA);
+                const uint32_t b_base = ptx::smem_u32(sB);
+                for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+                    for (int g = 0; g < G; ++g, ++it) {
+                        const uint32_t buf = it & 1u;
+                        const uint32_t bphase = (it >> 1) & 1u;
+                        if (!ptx::mbar_wait(&tempty[buf], bphase ^ 1u, abort_flag, args.err, ERRBIT_MMA_TMEM,
+                                            WAIT_TIMEOUT_NS) ||
+                            !ptx::mbar_wait(&full[stage], phase, abort_flag, args.err, ERRBIT_MMA_SMEM,
+                                            WAIT_TIMEOUT_NS)) {
+                            ok = false;
+                            break;
+                        }
+                        ptx::tc_fence_after();
+                        const uint64_t adesc = ptx::smem_desc_sw128_kmajor(a_base + stage * L::A_BYTES);
+                        const uint64_t bdesc = ptx::smem_desc_sw128_kmajor(b_base + stage * L::B_BYTES);
+                        const uint32_t d_tmem = tmem_base + buf * BN;
+#pragma unroll
+                        for (int j = 0; j < BK / 32; ++j)   // 32 bytes of K per instruction: +2 in the >>4 field
+                            ptx::mma_f8(d_tmem, adesc + 2 * j, bdesc + 2 * j, IDESC, j > 0 ? 1u : 0u);
+                        ptx::mma_commit(&empty[stage]);
+                        ptx::mma_commit(&tfull[buf]);
+                        if (++stage == STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                }
+                // all MMAs issued by this thread complete before teardown
+                ptx::mma_commit(mma_done);
+                ptx::mbar_wait(mma_done, 0, nullptr, args.err, ERRBIT_DRAIN, WAIT_TIMEOUT_NS);
+            }
+            __syncwarp();
+        } else if (warp == SCALE_WARP) {
+            // -------------------------------------------------- scale loader
+            int ss = 0;
+            uint32_t sphase = 0;
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
                 int tm, tn;
                 tile_coords(tile, args.tiles_m, args.tiles_n, tm, tn);
                 for (int g = 0; g < G; ++g) {
-                    if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, args.err, ERRBIT_PRODUCER,
+                    if (!ptx::mbar_wait(&sempty[ss], sphase ^ 1u, abort_flag, args.err, ERRBIT_PROMOTE,
                                         WAIT_TIMEOUT_NS)) {
                         ok = false;
                         break;
                     }
-                    ptx::mbar_arrive_expect_tx(&full[stage], L::STAGE_BYTES);
-                    ptx::tma_load_2d(sA + stage * L::A_BYTES, &tmap_a, &full[stage], g * BK, tm * BM);
-                    ptx::tma_load_2d(sB + stage * L::B_BYTES, &tmap_b, &full[stage], g * BK, tn * BN);
-                    issued_mask |= 1u << stage;
-                    issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-            }
-            if (!ok) {
-                // drain: every copy this thread started must land before exit
-                for (int s = 0; s < STAGES; ++s)
-                    if (issued_mask & (1u << s))
-                        ptx::mbar_wait(&full[s], (issued_parity >> s) & 1u, nullptr, args.err, ERRBIT_DRAIN,
-                                       WAIT_TIMEOUT_NS);
-            }
-        }
-        __syncwarp();
-      } else if (warp == MMA_WARP) {
-        // ------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
-            uint32_t it = 0;   // global group counter -> TMEM buffer / phase
-            bool ok = true;
-            const uint32_t a_base = ptx::smem_u32(sA);
-            const uint32_t b_base = ptx::smem_u32(sB);
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-                for (int g = 0; g < G; ++g, ++it) {
-                    const uint32_t buf = it & 1u;
-                    const uint32_t bphase = (it >> 1) & 1u;
-                    if (!ptx::mbar_wait(&tempty[buf], bphase ^ 1u, abort_flag, args.err, ERRBIT_MMA_TMEM,
-                                        WAIT_TIMEOUT_NS) ||
-                        !ptx::mbar_wait(&full[stage], phase, abort_flag, args.err, ERRBIT_MMA_SMEM,
-                                        WAIT_TIMEOUT_NS)) {
-                        ok = false;
-                        break;
-                    }
-                    ptx::tc_fence_after();
-                    const uint64_t adesc = ptx::smem_desc_sw128_kmajor(a_base + stage * L::A_BYTES);
-                    const uint64_t bdesc = ptx::smem_desc_sw128_kmajor(b_base + stage * L::B_BYTES);
-                    const uint32_t d_tmem = tmem_base + buf * BN;
+                    float *dst = scl + ss * L::SCALE_FLOATS;
+                    const float *sa_g = args.sa + static_cast<int64_t>(g) * args.rows;
 #pragma unroll
-                    for (int j = 0; j < BK / 32; ++j)   // K = 32 bytes per instruction: +2 in the >>4 address field
-                        ptx::mma_f8(d_tmem, adesc + 2 * j, bdesc + 2 * j, IDESC, j > 0 ? 1u : 0u);
-                    ptx::mma_commit(&empty[stage]);
-                    ptx::mma_commit(&tfull[buf]);
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
+                    for (int i = 0; i < BM / 32; ++i) {
+                        const int r = i * 32 + lane;
+                        const int row = tm * BM + r;
+                        const bool in = row < args.rows;
+                        ptx::cp_async_4(dst + r, in ? sa_g + row : args.sa, in ? 4u : 0u);
+                    }
+                    const float *sb_g = args.sb + static_cast<int64_t>(g) * args.sb_stride_g;
+                    if (SB_PER_COLUMN) {
+#pragma unroll
+                        for (int i = 0; i < BN / 128; ++i) {         // BN/4 16-byte pieces per slot
+                            const int c = (i * 32 + lane) * 4;
+                            const int col = tn * BN + c;
+                            const bool in = col < args.cols;
+                            ptx::cp_async_16z(dst + BM + c, in ? sb_g + col : args.sb, in ? 16u : 0u);
+                        }
+                    } else if (lane < BN / 128) {
+                        const int col = tn * BN + lane * 128;
+                        const bool in = col < args.cols;
+                        ptx::cp_async_4(dst + BM + lane,
+                                        in ? sb_g + static_cast<int64_t>(col >> 7) * args.sb_stride_c : args.sb,
+                                        in ? 4u : 0u);
+                    }
+                    ptx::cp_async_mbar_arrive_noinc(&sfull[ss]);
+                    if (++ss == SCALE_STAGES) {
+                        ss = 0;
+                        sphase ^= 1u;
                     }
                 }
             }
-            // all MMAs issued by this thread complete before teardown
-            ptx::mma_commit(mma_done);
-            ptx::mbar_wait(mma_done, 0, nullptr, args.err, ERRBIT_DRAIN, WAIT_TIMEOUT_NS);
+            ptx::cp_async_wait_all();
         }
-        __syncwarp();
-      }
     } else {
         ptx::setmaxnreg_inc<PROMO_REGS>();
         // ------------------------------------------------------ promotion
         const int wg = (warp - FIRST_PROMO_WARP) >> 2;   // 0 or 1: column half of the tile
-        const int quarter = warp & 3;         // TMEM lanes 32*quarter .. +31
+        const int quarter = warp & 3;                    // TMEM lanes 32*quarter .. +31
         const int row_in_tile = quarter * 32 + lane;
-        float *my_sb = reinterpret_cast<float *>(smem + L::SB_OFF) + (warp - FIRST_PROMO_WARP) * 2 * COLS_PER_WG;
         uint32_t it = 0;
+        int ss = 0;
+        uint32_t sphase = 0;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
             int tm, tn;
             tile_coords(tile, args.tiles_m, args.tiles_n, tm, tn);
             const int row = tm * BM + row_in_tile;
-            const bool row_ok = row < args.rows;
             const int col0 = tn * BN + wg * COLS_PER_WG;
-            const bool cols_ok = col0 < args.cols;
             float acc[COLS_PER_WG];
 #pragma unroll
             for (int i = 0; i < COLS_PER_WG; ++i)
                 acc[i] = 0.0f;
 
-            // Per-column scales (Wgrad): each warp copies its 128 (or 64) scales of
-            // group g+1 into its own smem buffer while it promotes group g.
-            auto prefetch_sb = [&](int g) {
-                if (SB_PER_COLUMN) {
-                    __syncwarp();
-                    constexpr int CHUNKS16 = COLS_PER_WG / 4;   // 16-byte pieces
-                    if (cols_ok && lane < CHUNKS16)
-                        ptx::cp_async_16(my_sb + (g & 1) * COLS_PER_WG + 4 * lane,
-                                         args.sb + static_cast<int64_t>(g) * args.sb_stride_g + col0 + 4 * lane);
-                    ptx::cp_async_commit();
-                }
-            };
-            prefetch_sb(0);
-            float sa_next = row_ok ? __ldg(args.sa + row) : 0.0f;
             for (int g = 0; g < G; ++g, ++it) {
                 const uint32_t buf = it & 1u;
                 const uint32_t bphase = (it >> 1) & 1u;
-                const float sa = sa_next;
-                if (g + 1 < G)
-                    sa_next = row_ok ? __ldg(args.sa + static_cast<int64_t>(g + 1) * args.rows + row) : 0.0f;
+                if (!ptx::mbar_wait(&sfull[ss], sphase, abort_flag, args.err, ERRBIT_PROMOTE, WAIT_TIMEOUT_NS)) {
+                    ok = false;
+                    break;
+                }
+                const float *scur = scl + ss * L::SCALE_FLOATS;
+                const float sa = scur[row_in_tile];
+                const float *sbcol = scur + BM + wg * COLS_PER_WG;
                 float w_blk = 0.0f;
                 if (!SB_PER_COLUMN) {
-                    const float *sbg = args.sb + static_cast<int64_t>(g) * args.sb_stride_g;
-                    w_blk = sa * (cols_ok ? __ldg(sbg + static_cast<int64_t>(col0 >> 7) * args.sb_stride_c) : 0.0f);
-                } else {
-                    if (g + 1 < G)
-                        prefetch_sb(g + 1);
-                    else
-                        ptx::cp_async_commit();          // keep one group in flight for the wait below
-                    ptx::cp_async_wait<1>();             // group g's scales have landed
+                    w_blk = sa * scur[BM + (wg * COLS_PER_WG) / 128];
                     __syncwarp();
+                    if (lane == 0)
+                        ptx::mbar_arrive(&sempty[ss]);
                 }
-                const float *sb_cur = my_sb + (g & 1) * COLS_PER_WG;
 
                 if (!ptx::mbar_wait(&tfull[buf], bphase, abort_flag, args.err, ERRBIT_PROMOTE, WAIT_TIMEOUT_NS)) {
                     ok = false;
@@ -310,7 +352,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                             ptx::mbar_arrive(&tempty[buf]);
                     }
                     if (SB_PER_COLUMN) {
-                        const float4 *sbv = reinterpret_cast<const float4 *>(sb_cur + c * 32);
+                        const float4 *sbv = reinterpret_cast<const float4 *>(sbcol + c * 32);
 #pragma unroll
                         for (int v = 0; v < 8; ++v) {
                             const float4 s4 = sbv[v];
@@ -327,10 +369,19 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                     if (c + 1 < CHUNKS)
                         ptx::tmem_ld_wait(p[(c + 1) & 1]);
                 }
+                if (SB_PER_COLUMN) {
+                    __syncwarp();
+                    if (lane == 0)
+                        ptx::mbar_arrive(&sempty[ss]);
+                }
+                if (++ss == SCALE_STAGES) {
+                    ss = 0;
+                    sphase ^= 1u;
+                }
             }
             if (!ok)
                 break;
-            if (row_ok && cols_ok) {
+            if (row < args.rows && col0 < args.cols) {
                 uint4 *dst = reinterpret_cast<uint4 *>(args.d + static_cast<int64_t>(row) * args.cols + col0);
 #pragma unroll
                 for (int v = 0; v < COLS_PER_WG / 8; ++v) {

@@ -115,6 +115,35 @@ __device__ __forceinline__ void cp_async_commit()
     asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
+// 4-byte asynchronous copy; with src_bytes == 0 nothing is read and the
+// destination is zero-filled.
+__device__ __forceinline__ void cp_async_4(void *smem_dst, const void *gmem_src, uint32_t src_bytes)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+
+// 16-byte variant with the same zero-fill rule (src_bytes 0 or 16).
+__device__ __forceinline__ void cp_async_16z(void *smem_dst, const void *gmem_src, uint32_t src_bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+
+// Arrive on `bar` once all of this thread's earlier cp.async copies have
+// completed; the arrival counts towards the barrier's expected count.
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t *bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all()
+{
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // Wait until at most N of this thread's committed groups are still pending.
 template <int N>
 __device__ __forceinline__ void cp_async_wait()

@@ -11,7 +11,9 @@
 // All three kernels are HBM-streaming: 16-byte vector loads, warp-shuffle
 // amax reductions, and stores arranged so that every written sector is full.
 // Compiled without fast-math so that `/` is the correctly rounded IEEE
-// division and subnormals are kept.
+// division and subnormals are kept; the per-element division itself is
+// replaced by an exact bracketing test (see encode2), with the division as the
+// rare fallback.
 #include <cuda_runtime.h>
 #include <cstdint>
 
@@ -41,19 +43,56 @@ __device__ __forceinline__ float absmax8(const float (&f)[8])
     return a;
 }
 
-// Codes for 4 consecutive values, little-endian in one word (value i in byte i).
-__device__ __forceinline__ uint32_t encode4(float a, float b, float c, float d, float s)
+// Exact E4M3 codes of fp32(x / s) without a division per element.
+//
+// With r = RN(1/s) (IEEE reciprocal), ra = RN(r (1 - 2^-21)) and
+// rb = RN(r (1 + 2^-21)), the products va = RN(x ra) and vb = RN(x rb) satisfy
+// |va| < |x/s| < |vb| (same sign): each carries at most three roundings of
+// relative size 2^-24, which the 2^-21 margin outweighs.  Round-to-nearest-even
+// with saturation is monotone, so every fp32 value between va and vb -- in
+// particular fp32(x/s) -- has the same E4M3 code whenever va and vb do.  Only
+// when they differ (x/s within ~2^-21 of a rounding midpoint, or exactly on
+// one) is the correctly rounded quotient x / s computed.  A subnormal scale
+// (1/s would overflow) always takes the division.
+struct GroupScale {
+    float s, ra, rb;
+    bool fast;
+};
+
+__device__ __forceinline__ GroupScale group_scale(float amax)
 {
-    const uint32_t lo = ptx::cvt_e4m3x2(a / s, b / s);
-    const uint32_t hi = ptx::cvt_e4m3x2(c / s, d / s);
-    return lo | (hi << 16);
+    GroupScale g;
+    g.s = amax / 448.0f;
+    g.fast = g.s >= 1.17549435e-38f;        // smallest normal fp32
+    const float r = __frcp_rn(g.fast ? g.s : 1.0f);
+    g.ra = r * 0x1.fffffp-1f;              // 1 - 2^-21
+    g.rb = r * 0x1.000008p+0f;             // 1 + 2^-21
+    return g;
 }
 
-__device__ __forceinline__ uint2 encode8(const float (&f)[8], float s)
+// Codes of two values: lo's code in bits 0..7, hi's in bits 8..15.
+__device__ __forceinline__ uint32_t encode2(float lo, float hi, const GroupScale &g)
 {
-    if (s == 0.0f)
+    if (g.fast) {
+        const uint32_t a = ptx::cvt_e4m3x2(lo * g.ra, hi * g.ra);
+        const uint32_t b = ptx::cvt_e4m3x2(lo * g.rb, hi * g.rb);
+        if (a == b)
+            return a;
+    }
+    return ptx::cvt_e4m3x2(lo / g.s, hi / g.s);
+}
+
+// Codes for 4 consecutive values, little-endian in one word (value i in byte i).
+__device__ __forceinline__ uint32_t encode4(float a, float b, float c, float d, const GroupScale &g)
+{
+    return encode2(a, b, g) | (encode2(c, d, g) << 16);
+}
+
+__device__ __forceinline__ uint2 encode8(const float (&f)[8], const GroupScale &g)
+{
+    if (g.s == 0.0f)
         return make_uint2(0u, 0u);
-    return make_uint2(encode4(f[0], f[1], f[2], f[3], s), encode4(f[4], f[5], f[6], f[7], s));
+    return make_uint2(encode4(f[0], f[1], f[2], f[3], g), encode4(f[4], f[5], f[6], f[7], g));
 }
 
 // ---------------------------------------------------------------------------
@@ -104,12 +143,12 @@ quantize_act_kernel(const uint4 *__restrict__ x, int64_t M, int64_t K, uint2 *__
 #pragma unroll
             for (int o = 8; o >= 1; o >>= 1)
                 amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-            const float sc = amax / 448.0f;
-            const uint2 codes = encode8(f, sc);
+            const GroupScale gs = group_scale(amax);
+            const uint2 codes = encode8(f, gs);
             if (m < M && g < G)
                 __stcs(q + m * K8 + g * 16 + sub, codes);
             if (sub == 0)
-                s_tile[2 * j + half][warp + 8 * i] = sc;
+                s_tile[2 * j + half][warp + 8 * i] = gs.s;
         }
     }
     __syncthreads();
@@ -175,23 +214,23 @@ quantize_act_t_kernel(const uint4 *__restrict__ x, int64_t M, int64_t C, uint8_t
     s_amax[qd][c] = amax;
     __syncthreads();
     amax = fmaxf(fmaxf(s_amax[0][c], s_amax[1][c]), fmaxf(s_amax[2][c], s_amax[3][c]));
-    const float sc = amax / 448.0f;
+    const GroupScale gs = group_scale(amax);
 
     uint32_t w[8];
-    if (sc == 0.0f) {
+    if (gs.s == 0.0f) {
 #pragma unroll
         for (int i = 0; i < 8; ++i)
             w[i] = 0u;
     } else {
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-            w[i] = encode4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3], sc);
+            w[i] = encode4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3], gs);
     }
     uint4 *dst = reinterpret_cast<uint4 *>(qt + (c0 + c) * M + m0 + 32 * qd);
     __stcs(dst, make_uint4(w[0], w[1], w[2], w[3]));
     __stcs(dst + 1, make_uint4(w[4], w[5], w[6], w[7]));
     if (qd == 0)
-        st[(m0 >> 7) * C + c0 + c] = sc;
+        st[(m0 >> 7) * C + c0 + c] = gs.s;
 }
 
 // ---------------------------------------------------------------------------
@@ -235,15 +274,15 @@ quantize_weight_kernel(const uint4 *__restrict__ w, int64_t N, int64_t K, uint2 
 #pragma unroll
     for (int i = 1; i < Q3_THREADS / 32; ++i)
         amax = fmaxf(amax, s_red[i]);
-    const float sc = amax / 448.0f;
+    const GroupScale gs = group_scale(amax);
     if (t == 0)
-        s[bn * (K >> 7) + bk] = sc;
+        s[bn * (K >> 7) + bk] = gs.s;
 
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         float f[8];
         unpack8(v[i], f);
-        const uint2 codes = encode8(f, sc);
+        const uint2 codes = encode8(f, gs);
         const int r = r0 + 16 * i;
         __stcs(q + (bn * 128 + r) * K8 + bk * 16 + sub, codes);
         if (qt != nullptr)

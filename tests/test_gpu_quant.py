@@ -2,8 +2,9 @@
 
 Covers tiny and ragged shapes (tails of every tile), special values (zero
 groups, bf16 subnormals, signed zeros, saturation, outlier channels), the
-8B-class layer shapes at full size, and the E4M3 convert itself over large
-slices of all fp32 bit patterns.
+8B-class layer shapes at full size, values placed on and next to E4M3
+rounding midpoints, and the conversion of every finite bf16 value |x| <= 448
+(groups whose scale is exactly 1).
 """
 import numpy as np
 import pytest
@@ -99,6 +100,63 @@ def test_quantize_weight_special_values():
     assert_bitexact(q, oq, "codes")
     assert_bitexact(s, os_, "scales")
     assert_bitexact(qt, oqt, "transposed codes")
+
+
+def tie_groups(rows, seed):
+    """Groups made to hit E4M3 rounding midpoints: amax = 448 * 2^e (an exact
+    power-of-two scale), the other values exact midpoints between neighbouring
+    E4M3 values times 2^e, and their bf16 neighbours -- every value lands on
+    or next to a rounding boundary, exercising the exact-division fallback."""
+    codes = torch.arange(0, 0x7F, dtype=torch.int32).to(torch.uint8)
+    vals = codes.view(torch.float8_e4m3fn).float()
+    mids = (vals[:-1] + vals[1:]) / 2
+    g = torch.Generator().manual_seed(seed)
+    out = torch.empty(rows, 128)
+    for r in range(rows):
+        e = int(torch.randint(-30, 10, (1,), generator=g))
+        pick = mids[torch.randint(0, mids.numel(), (127,), generator=g)]
+        sign = torch.where(torch.rand(127, generator=g) < 0.5, -1.0, 1.0)
+        row = torch.cat([torch.tensor([448.0]), pick * sign]) * 2.0 ** e
+        out[r] = row
+    x = out.to(torch.bfloat16)
+    # nudge a third of the entries to a bf16 neighbour of the midpoint
+    bits = x.view(torch.int16)
+    nudge = (torch.randint(0, 3, bits.shape, generator=g) - 1).to(torch.int16)
+    nudge[:, 0] = 0
+    return (bits + nudge).view(torch.bfloat16)
+
+
+def test_rounding_midpoints_all_quantisers():
+    x = tie_groups(256, 9)                                     # [256, 128]
+    q, s = jf.quantize_act(x.to(DEV))
+    oq, os_ = oracle.quantize_act(bits(x))
+    assert_bitexact(q, oq, "act codes")
+    assert_bitexact(s, os_, "act scales")
+    xt = x.T.contiguous()                                      # [128, 256]: groups along rows
+    qt, st = jf.quantize_act_transposed(xt.to(DEV))
+    oqt, ost = oracle.quantize_act_transposed(bits(xt))
+    assert_bitexact(qt, oqt, "transposed codes")
+    w = x[:128].reshape(128, 128).contiguous()
+    w[0, 0] = 448.0 * 2.0 ** 5                                  # one pow2 scale for the block
+    qw, sw, qwt = jf.quantize_weight(w.to(DEV))
+    oqw, osw, oqwt = oracle.quantize_weight(bits(w), True)
+    assert_bitexact(qw, oqw, "weight codes")
+    assert_bitexact(qwt, oqwt, "weight transposed codes")
+
+
+def test_all_bf16_values_scale_one():
+    """Every finite bf16 value with |x| <= 448 in groups whose amax is 448, so
+    s = 1 and the code is the E4M3 rounding of x itself."""
+    allb = torch.arange(-32768, 32768, dtype=torch.int32).to(torch.int16).view(torch.bfloat16).float()
+    v = allb[torch.isfinite(allb) & (allb.abs() <= 448.0)]
+    n = (v.numel() + 126) // 127 * 127
+    pad = torch.zeros(n)
+    pad[:v.numel()] = v
+    x = torch.cat([torch.full((n // 127, 1), 448.0), pad.view(-1, 127)], dim=1).to(torch.bfloat16)
+    q, s = jf.quantize_act(x.to(DEV))
+    oq, os_ = oracle.quantize_act(bits(x))
+    assert np.all(os_ == 1.0)
+    assert_bitexact(q, oq, "codes")
 
 
 def test_empty_inputs():

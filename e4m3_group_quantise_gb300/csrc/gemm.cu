@@ -113,6 +113,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     using L = Smem<BN, STAGES>;
     constexpr int COLS_PER_WG = BN / 2;          // columns per promotion warpgroup
     constexpr int CHUNKS = COLS_PER_WG / 32;     // tcgen05.ld x32 per group
+    static_assert(CHUNKS % 2 == 0, "loads are issued in pairs");
     constexpr uint32_t TMEM_COLS = 2 * BN;       // two partial buffers
     constexpr uint32_t IDESC = ptx::idesc_e4m3_f32(BM, BN);
 
@@ -336,38 +337,49 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                 ptx::tc_fence_after();
                 const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + buf * BN +
                                        wg * COLS_PER_WG;
-                uint32_t p[2][32];
-                ptx::tmem_ld_32x32b_x32(taddr, p[0]);
-                ptx::tmem_ld_wait(p[0]);
+                // Two 32-column loads in flight per wait (64 columns), so each
+                // group pays the TMEM load latency only COLS_PER_WG / 64 times.
 #pragma unroll
-                for (int c = 0; c < CHUNKS; ++c) {
-                    uint32_t(&cur)[32] = p[c & 1];
-                    if (c + 1 < CHUNKS) {
-                        ptx::tmem_ld_32x32b_x32(taddr + (c + 1) * 32, p[(c + 1) & 1]);
-                    } else {
+                for (int h = 0; h < CHUNKS / 2; ++h) {
+                    uint32_t p0[32], p1[32];
+                    ptx::tmem_ld_32x32b_x32(taddr + h * 64, p0);
+                    ptx::tmem_ld_32x32b_x32(taddr + h * 64 + 32, p1);
+                    ptx::tmem_ld_wait(p0);
+                    ptx::tmem_ld_wait(p1);
+                    if (h + 1 == CHUNKS / 2) {
                         // the whole partial is in registers: hand the buffer back
                         ptx::tc_fence_before();
                         __syncwarp();
                         if (lane == 0)
                             ptx::mbar_arrive(&tempty[buf]);
                     }
+                    float *a0 = acc + h * 64;
                     if (SB_PER_COLUMN) {
-                        const float4 *sbv = reinterpret_cast<const float4 *>(sbcol + c * 32);
+                        const float4 *sbv = reinterpret_cast<const float4 *>(sbcol + h * 64);
 #pragma unroll
                         for (int v = 0; v < 8; ++v) {
                             const float4 s4 = sbv[v];
-                            acc[c * 32 + 4 * v + 0] = fmaf(__uint_as_float(cur[4 * v + 0]), sa * s4.x, acc[c * 32 + 4 * v + 0]);
-                            acc[c * 32 + 4 * v + 1] = fmaf(__uint_as_float(cur[4 * v + 1]), sa * s4.y, acc[c * 32 + 4 * v + 1]);
-                            acc[c * 32 + 4 * v + 2] = fmaf(__uint_as_float(cur[4 * v + 2]), sa * s4.z, acc[c * 32 + 4 * v + 2]);
-                            acc[c * 32 + 4 * v + 3] = fmaf(__uint_as_float(cur[4 * v + 3]), sa * s4.w, acc[c * 32 + 4 * v + 3]);
+                            a0[4 * v + 0] = fmaf(__uint_as_float(p0[4 * v + 0]), sa * s4.x, a0[4 * v + 0]);
+                            a0[4 * v + 1] = fmaf(__uint_as_float(p0[4 * v + 1]), sa * s4.y, a0[4 * v + 1]);
+                            a0[4 * v + 2] = fmaf(__uint_as_float(p0[4 * v + 2]), sa * s4.z, a0[4 * v + 2]);
+                            a0[4 * v + 3] = fmaf(__uint_as_float(p0[4 * v + 3]), sa * s4.w, a0[4 * v + 3]);
+                        }
+#pragma unroll
+                        for (int v = 0; v < 8; ++v) {
+                            const float4 s4 = sbv[8 + v];
+                            a0[32 + 4 * v + 0] = fmaf(__uint_as_float(p1[4 * v + 0]), sa * s4.x, a0[32 + 4 * v + 0]);
+                            a0[32 + 4 * v + 1] = fmaf(__uint_as_float(p1[4 * v + 1]), sa * s4.y, a0[32 + 4 * v + 1]);
+                            a0[32 + 4 * v + 2] = fmaf(__uint_as_float(p1[4 * v + 2]), sa * s4.z, a0[32 + 4 * v + 2]);
+                            a0[32 + 4 * v + 3] = fmaf(__uint_as_float(p1[4 * v + 3]), sa * s4.w, a0[32 + 4 * v + 3]);
                         }
                     } else {
 #pragma unroll
                         for (int i = 0; i < 32; ++i)
-                            acc[c * 32 + i] = fmaf(__uint_as_float(cur[i]), w_blk, acc[c * 32 + i]);
+                            a0[i] = fmaf(__uint_as_float(p0[i]), w_blk, a0[i]);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            a0[32 + i] = fmaf(__uint_as_float(p1[i]), w_blk, a0[32 + i]);
                     }
-                    if (c + 1 < CHUNKS)
-                        ptx::tmem_ld_wait(p[(c + 1) & 1]);
                 }
                 if (SB_PER_COLUMN) {
                     __syncwarp();

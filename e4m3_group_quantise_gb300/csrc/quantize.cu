@@ -70,93 +70,112 @@ __device__ __forceinline__ GroupScale group_scale(float amax)
     return g;
 }
 
-// Codes of two values: lo's code in bits 0..7, hi's in bits 8..15.
-__device__ __forceinline__ uint32_t encode2(float lo, float hi, const GroupScale &g)
+// Codes of two values (lo's code in bits 0..7, hi's in bits 8..15) from the
+// lower bracket end; `mism` collects any disagreement with the upper end.
+__device__ __forceinline__ uint32_t encode2_fast(float lo, float hi, const GroupScale &g, uint32_t &mism)
 {
-    if (g.fast) {
-        const uint32_t a = ptx::cvt_e4m3x2(lo * g.ra, hi * g.ra);
-        const uint32_t b = ptx::cvt_e4m3x2(lo * g.rb, hi * g.rb);
-        if (a == b)
-            return a;
+    const uint32_t a = ptx::cvt_e4m3x2(lo * g.ra, hi * g.ra);
+    const uint32_t b = ptx::cvt_e4m3x2(lo * g.rb, hi * g.rb);
+    mism |= a ^ b;
+    return a;
+}
+
+// The same codes through the correctly rounded quotient.
+__device__ __forceinline__ uint32_t encode2_exact(float lo, float hi, float s)
+{
+    return ptx::cvt_e4m3x2(lo / s, hi / s);
+}
+
+// Codes of N consecutive values (N % 4 == 0) into N/4 little-endian words:
+// the bracket test first, the exact quotient for the whole run only if any
+// pair's bracket ends disagree (or the scale is subnormal).  A zero scale
+// (all-zero group) gives zero codes.
+template <int N>
+__device__ __forceinline__ void encode_run(const float *f, const GroupScale &g, uint32_t *w)
+{
+    if (g.s == 0.0f) {
+#pragma unroll
+        for (int i = 0; i < N / 4; ++i)
+            w[i] = 0u;
+        return;
     }
-    return ptx::cvt_e4m3x2(lo / g.s, hi / g.s);
-}
-
-// Codes for 4 consecutive values, little-endian in one word (value i in byte i).
-__device__ __forceinline__ uint32_t encode4(float a, float b, float c, float d, const GroupScale &g)
-{
-    return encode2(a, b, g) | (encode2(c, d, g) << 16);
-}
-
-__device__ __forceinline__ uint2 encode8(const float (&f)[8], const GroupScale &g)
-{
-    if (g.s == 0.0f)
-        return make_uint2(0u, 0u);
-    return make_uint2(encode4(f[0], f[1], f[2], f[3], g), encode4(f[4], f[5], f[6], f[7], g));
+    uint32_t mism = g.fast ? 0u : 1u;
+    if (g.fast) {
+#pragma unroll
+        for (int i = 0; i < N / 4; ++i)
+            w[i] = encode2_fast(f[4 * i], f[4 * i + 1], g, mism) |
+                   (encode2_fast(f[4 * i + 2], f[4 * i + 3], g, mism) << 16);
+    }
+    if (mism != 0u) {
+#pragma unroll
+        for (int i = 0; i < N / 4; ++i)
+            w[i] = encode2_exact(f[4 * i], f[4 * i + 1], g.s) | (encode2_exact(f[4 * i + 2], f[4 * i + 3], g.s) << 16);
+    }
 }
 
 // ---------------------------------------------------------------------------
-// 1x128 groups along rows.  CTA tile: 32 rows x 8 groups (1024 columns).
-// Warp w owns rows w, w+8, w+16, w+24; each half-warp owns one group of a
-// row per step (16 lanes x 8 values).  Scales are staged in shared memory and
-// written group-major, 32 consecutive rows (128 bytes) per group.
+// 1x128 groups along rows.  CTA tile: 16 rows x 8 groups (1024 columns).
+// Warp w owns group g0 + w of 8 rows at a time; four lanes share a group
+// (lane = 4 * row + sub), each holding 32 values: 16-byte chunks sub, sub+4,
+// sub+8, sub+12 of the group's 256 bytes.  Every load instruction reads 64
+// contiguous bytes per row, every code store writes 32 (one full sector),
+// and the 8 rows' scales of one group are contiguous (group-major), so
+// lanes with sub == 0 store them as one 32-byte sector -- no shared memory.
+// The amax needs two shuffles; the scale arithmetic is shared by 32 values.
 // ---------------------------------------------------------------------------
-constexpr int Q1_ROWS = 32;
+constexpr int Q1_ROWS = 16;
 constexpr int Q1_GROUPS = 8;
 constexpr int Q1_THREADS = 256;
 
-__global__ void __launch_bounds__(Q1_THREADS)
+__global__ void __launch_bounds__(Q1_THREADS, 4)
 quantize_act_kernel(const uint4 *__restrict__ x, int64_t M, int64_t K, uint2 *__restrict__ q,
                     float *__restrict__ s)
 {
-    __shared__ float s_tile[Q1_GROUPS][Q1_ROWS];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int half = lane >> 4, sub = lane & 15;
+    const int r = lane >> 2, sub = lane & 3;
     const int64_t G = K >> 7;
     const int64_t m0 = static_cast<int64_t>(blockIdx.x) * Q1_ROWS;
-    const int64_t g0 = static_cast<int64_t>(blockIdx.y) * Q1_GROUPS;
-    const int64_t K8 = K >> 3;   // 16-byte chunks per bf16 row (8 codes per uint2 chunk as well)
+    const int64_t g = static_cast<int64_t>(blockIdx.y) * Q1_GROUPS + warp;
+    const int64_t K8 = K >> 3;   // 16-byte bf16 chunks per row (= 8-byte code chunks per row)
+    if (g >= G)
+        return;
 
-    uint4 v[4][4];
+    uint4 v[2][4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int64_t m = m0 + warp + 8 * i;
+    for (int b = 0; b < 2; ++b) {
+        const int64_t m = m0 + 8 * b + r;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int64_t g = g0 + 2 * j + half;
-            if (m < M && g < G)
-                v[i][j] = __ldcs(x + m * K8 + g * 16 + sub);
-            else
-                v[i][j] = make_uint4(0u, 0u, 0u, 0u);
-        }
+        for (int j = 0; j < 4; ++j)
+            v[b][j] = (m < M) ? __ldcs(x + m * K8 + g * 16 + 4 * j + sub) : make_uint4(0u, 0u, 0u, 0u);
     }
-
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int64_t m = m0 + warp + 8 * i;
+    for (int b = 0; b < 2; ++b) {
+        const int64_t m = m0 + 8 * b + r;
+        float f[32];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const int64_t g = g0 + 2 * j + half;
-            float f[8];
-            unpack8(v[i][j], f);
-            float amax = absmax8(f);
+            float t[8];
+            unpack8(v[b][j], t);
 #pragma unroll
-            for (int o = 8; o >= 1; o >>= 1)
-                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-            const GroupScale gs = group_scale(amax);
-            const uint2 codes = encode8(f, gs);
-            if (m < M && g < G)
-                __stcs(q + m * K8 + g * 16 + sub, codes);
+            for (int e = 0; e < 8; ++e)
+                f[8 * j + e] = t[e];
+        }
+        float amax = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+            amax = fmaxf(amax, fabsf(f[e]));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        const GroupScale gs = group_scale(amax);
+        uint32_t w[8];
+        encode_run<32>(f, gs, w);
+        if (m < M) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                __stcs(q + m * K8 + g * 16 + 4 * j + sub, make_uint2(w[2 * j], w[2 * j + 1]));
             if (sub == 0)
-                s_tile[2 * j + half][warp + 8 * i] = gs.s;
+                s[g * M + m] = gs.s;
         }
-    }
-    __syncthreads();
-    {
-        const int gl = threadIdx.x >> 5, r = threadIdx.x & 31;
-        const int64_t g = g0 + gl, m = m0 + r;
-        if (g < G && m < M)
-            s[g * M + m] = s_tile[gl][r];
     }
 }
 
@@ -217,15 +236,7 @@ quantize_act_t_kernel(const uint4 *__restrict__ x, int64_t M, int64_t C, uint8_t
     const GroupScale gs = group_scale(amax);
 
     uint32_t w[8];
-    if (gs.s == 0.0f) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            w[i] = 0u;
-    } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            w[i] = encode4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3], gs);
-    }
+    encode_run<32>(f, gs, w);
     uint4 *dst = reinterpret_cast<uint4 *>(qt + (c0 + c) * M + m0 + 32 * qd);
     __stcs(dst, make_uint4(w[0], w[1], w[2], w[3]));
     __stcs(dst + 1, make_uint4(w[4], w[5], w[6], w[7]));
@@ -282,7 +293,9 @@ quantize_weight_kernel(const uint4 *__restrict__ w, int64_t N, int64_t K, uint2 
     for (int i = 0; i < 8; ++i) {
         float f[8];
         unpack8(v[i], f);
-        const uint2 codes = encode8(f, gs);
+        uint32_t w[2];
+        encode_run<8>(f, gs, w);
+        const uint2 codes = make_uint2(w[0], w[1]);
         const int r = r0 + 16 * i;
         __stcs(q + (bn * 128 + r) * K8 + bk * 16 + sub, codes);
         if (qt != nullptr)

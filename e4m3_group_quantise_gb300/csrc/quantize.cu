@@ -127,7 +127,7 @@ constexpr int Q1_ROWS = 16;
 constexpr int Q1_GROUPS = 8;
 constexpr int Q1_THREADS = 256;
 
-__global__ void __launch_bounds__(Q1_THREADS, 4)
+__global__ void __launch_bounds__(Q1_THREADS)
 quantize_act_kernel(const uint4 *__restrict__ x, int64_t M, int64_t K, uint2 *__restrict__ q,
                     float *__restrict__ s)
 {

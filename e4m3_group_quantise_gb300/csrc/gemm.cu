@@ -21,14 +21,21 @@
 //
 // Structure: persistent, one CTA per SM, 384 threads (3 warpgroups).
 //   warp 0, lane 0 : TMA producer   -- A and B tiles of one group per smem stage
-//   warp 1, lane 0 : MMA issuer     -- 4 x tcgen05.mma (K = 32 each) per group
-//                                      into one of two TMEM partial buffers
+//   warp 1, lane 0 : MMA issuer     -- per group and per column half, 4 x
+//                                      tcgen05.mma (N = BN/2, K = 32 each) into
+//                                      one of four TMEM partial buffers
 //   warp 2         : scale loader   -- cp.async of the group's row scales (128)
 //                                      and column scales into a smem ring
-//   warps 4..11    : promotion      -- two warpgroups, each 128 rows x BN/2
-//                                      columns; tcgen05.ld the partial, free the
-//                                      buffer, acc += partial * sa * sb; bf16
-//                                      epilogue straight from registers
+//   warps 4..11    : promotion      -- two warpgroups, one per column half
+//                                      (128 rows x BN/2); tcgen05.ld the partial,
+//                                      free the buffer, acc += partial * sa * sb;
+//                                      bf16 epilogue: each warp stages 32 rows x
+//                                      16 columns in shared memory and TMA-stores
+//                                      them (double-buffered, asynchronous)
+// TMEM holds four BN/2-column partial buffers, two per half: the chain from an
+// MMA's completion through promotion's release to the next MMA into that
+// buffer (about 700 cycles measured) then overlaps three half-group MMAs
+// (768 cycles at BN = 256) instead of one.
 // Registers are rebalanced with setmaxnreg: the control warpgroup drops to 40
 // per thread and the promotion warpgroups rise to 232 (128*40 + 256*232 =
 // 64512 = 384 threads * 168, the launch allocation).
@@ -82,9 +89,13 @@ struct Smem {
     static constexpr uint32_t SCALE_FLOATS = BM + BN;
     static constexpr uint32_t SCALE_OFF = TILES;
     static constexpr uint32_t SCALE_BYTES = SCALE_STAGES * SCALE_FLOATS * 4;
-    static constexpr uint32_t BAR_OFF = SCALE_OFF + SCALE_BYTES;
-    // full[S], empty[S], sfull[SS], sempty[SS], tfull[2], tempty[2], mma_done, tmem holder, abort flag
-    static constexpr uint32_t CTRL_BYTES = (2 * STAGES + 2 * SCALE_STAGES + 5) * 8 + 16;
+    // epilogue staging: per promotion warp two 32-row x 16-column bf16 chunks
+    static constexpr uint32_t OUT_OFF = SCALE_OFF + SCALE_BYTES;
+    static constexpr uint32_t OUT_CHUNK_BYTES = 32 * 16 * 2;
+    static constexpr uint32_t OUT_BYTES = 8 * 2 * OUT_CHUNK_BYTES;
+    static constexpr uint32_t BAR_OFF = OUT_OFF + OUT_BYTES;
+    // full[S], empty[S], sfull[SS], sempty[SS], tfull[4], tempty[4], mma_done, tmem holder, abort flag
+    static constexpr uint32_t CTRL_BYTES = (2 * STAGES + 2 * SCALE_STAGES + 9) * 8 + 16;
     static constexpr uint32_t TOTAL = 1024 /* alignment slack */ + BAR_OFF + CTRL_BYTES;
 };
 
@@ -108,14 +119,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 template <int BN, int STAGES, bool SB_PER_COLUMN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-            const KernelArgs args)
+            const __grid_constant__ CUtensorMap tmap_d, const KernelArgs args)
 {
     using L = Smem<BN, STAGES>;
     constexpr int COLS_PER_WG = BN / 2;          // columns per promotion warpgroup
     constexpr int CHUNKS = COLS_PER_WG / 32;     // tcgen05.ld x32 per group
     static_assert(CHUNKS % 2 == 0, "loads are issued in pairs");
-    constexpr uint32_t TMEM_COLS = 2 * BN;       // two partial buffers
-    constexpr uint32_t IDESC = ptx::idesc_e4m3_f32(BM, BN);
+    constexpr int HALF = BN / 2;                  // columns per MMA half = per TMEM buffer
+    constexpr uint32_t TMEM_COLS = 4 * HALF;     // four partial buffers
+    constexpr uint32_t IDESC = ptx::idesc_e4m3_f32(BM, HALF);
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -127,8 +139,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     uint64_t *sfull = empty + STAGES;
     uint64_t *sempty = sfull + SCALE_STAGES;
     uint64_t *tfull = sempty + SCALE_STAGES;
-    uint64_t *tempty = tfull + 2;
-    uint64_t *mma_done = tempty + 2;
+    uint64_t *tempty = tfull + 4;
+    uint64_t *mma_done = tempty + 4;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(mma_done + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
 
@@ -147,9 +159,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                 ptx::mbar_init(&sfull[s], 32);   // every loader lane's copies
                 ptx::mbar_init(&sempty[s], 8);   // one arrival per promotion warp
             }
-            for (int b = 0; b < 2; ++b) {
+            for (int b = 0; b < 4; ++b) {
                 ptx::mbar_init(&tfull[b], 1);
-                ptx::mbar_init(&tempty[b], 8);   // one arrival per promotion warp
+                ptx::mbar_init(&tempty[b], 4);   // one arrival per warp of the half's warpgroup
             }
             ptx::mbar_init(mma_done, 1);
             *abort_flag = 0;
@@ -215,24 +227,33 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                 const uint32_t b_base = ptx::smem_u32(sB);
                 for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
                     for (int g = 0; g < G; ++g, ++it) {
-                        const uint32_t buf = it & 1u;
                         const uint32_t bphase = (it >> 1) & 1u;
-                        if (!ptx::mbar_wait(&tempty[buf], bphase ^ 1u, abort_flag, args.err, ERRBIT_MMA_TMEM,
-                                            WAIT_TIMEOUT_NS) ||
-                            !ptx::mbar_wait(&full[stage], phase, abort_flag, args.err, ERRBIT_MMA_SMEM,
+                        if (!ptx::mbar_wait(&full[stage], phase, abort_flag, args.err, ERRBIT_MMA_SMEM,
                                             WAIT_TIMEOUT_NS)) {
                             ok = false;
                             break;
                         }
-                        ptx::tc_fence_after();
                         const uint64_t adesc = ptx::smem_desc_sw128_kmajor(a_base + stage * L::A_BYTES);
-                        const uint64_t bdesc = ptx::smem_desc_sw128_kmajor(b_base + stage * L::B_BYTES);
-                        const uint32_t d_tmem = tmem_base + buf * BN;
 #pragma unroll
-                        for (int j = 0; j < BK / 32; ++j)   // 32 bytes of K per instruction: +2 in the >>4 field
-                            ptx::mma_f8(d_tmem, adesc + 2 * j, bdesc + 2 * j, IDESC, j > 0 ? 1u : 0u);
+                        for (int h = 0; h < 2; ++h) {
+                            const uint32_t buf = ((it & 1u) << 1) | h;
+                            if (!ptx::mbar_wait(&tempty[buf], bphase ^ 1u, abort_flag, args.err, ERRBIT_MMA_TMEM,
+                                                WAIT_TIMEOUT_NS)) {
+                                ok = false;
+                                break;
+                            }
+                            ptx::tc_fence_after();
+                            const uint64_t bdesc =
+                                ptx::smem_desc_sw128_kmajor(b_base + stage * L::B_BYTES + h * HALF * BK);
+                            const uint32_t d_tmem = tmem_base + buf * HALF;
+#pragma unroll
+                            for (int j = 0; j < BK / 32; ++j)   // 32 bytes of K per instruction: +2 in the >>4 field
+                                ptx::mma_f8(d_tmem, adesc + 2 * j, bdesc + 2 * j, IDESC, j > 0 ? 1u : 0u);
+                            ptx::mma_commit(&tfull[buf]);
+                        }
+                        if (!ok)
+                            break;
                         ptx::mma_commit(&empty[stage]);
-                        ptx::mma_commit(&tfull[buf]);
                         if (++stage == STAGES) {
                             stage = 0;
                             phase ^= 1u;
@@ -298,6 +319,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         const int wg = (warp - FIRST_PROMO_WARP) >> 2;   // 0 or 1: column half of the tile
         const int quarter = warp & 3;                    // TMEM lanes 32*quarter .. +31
         const int row_in_tile = quarter * 32 + lane;
+        uint8_t *out_stage = smem + L::OUT_OFF + (warp - FIRST_PROMO_WARP) * 2 * L::OUT_CHUNK_BYTES;
         uint32_t it = 0;
         int ss = 0;
         uint32_t sphase = 0;
@@ -305,7 +327,6 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
             int tm, tn;
             tile_coords(tile, args.tiles_m, args.tiles_n, tm, tn);
-            const int row = tm * BM + row_in_tile;
             const int col0 = tn * BN + wg * COLS_PER_WG;
             float acc[COLS_PER_WG];
 #pragma unroll
@@ -313,7 +334,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                 acc[i] = 0.0f;
 
             for (int g = 0; g < G; ++g, ++it) {
-                const uint32_t buf = it & 1u;
+                const uint32_t buf = ((it & 1u) << 1) | wg;
                 const uint32_t bphase = (it >> 1) & 1u;
                 if (!ptx::mbar_wait(&sfull[ss], sphase, abort_flag, args.err, ERRBIT_PROMOTE, WAIT_TIMEOUT_NS)) {
                     ok = false;
@@ -335,8 +356,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                     break;
                 }
                 ptx::tc_fence_after();
-                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + buf * BN +
-                                       wg * COLS_PER_WG;
+                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + buf * HALF;
                 // Two 32-column loads in flight per wait (64 columns), so each
                 // group pays the TMEM load latency only COLS_PER_WG / 64 times.
 #pragma unroll
@@ -393,19 +413,40 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
             }
             if (!ok)
                 break;
-            if (row < args.rows && col0 < args.cols) {
-                uint4 *dst = reinterpret_cast<uint4 *>(args.d + static_cast<int64_t>(row) * args.cols + col0);
+            // Epilogue: bf16 rows of this warp (32 rows x COLS_PER_WG) leave through
+            // shared memory in 16-column chunks, each written by one TMA store
+            // (rows or columns past the tensor are clipped by the copy engine).
+            if (col0 < args.cols) {
 #pragma unroll
-                for (int v = 0; v < COLS_PER_WG / 8; ++v) {
-                    uint4 o;
-                    o.x = pack_bf16x2(acc[8 * v + 0], acc[8 * v + 1]);
-                    o.y = pack_bf16x2(acc[8 * v + 2], acc[8 * v + 3]);
-                    o.z = pack_bf16x2(acc[8 * v + 4], acc[8 * v + 5]);
-                    o.w = pack_bf16x2(acc[8 * v + 6], acc[8 * v + 7]);
-                    dst[v] = o;
+                for (int c = 0; c < COLS_PER_WG / 16; ++c) {
+                    uint8_t *chunk = out_stage + (c & 1) * L::OUT_CHUNK_BYTES;
+                    if (lane == 0)
+                        ptx::bulk_wait_read<1>();          // the store that last used this buffer has read it
+                    __syncwarp();
+                    uint4 *dst = reinterpret_cast<uint4 *>(chunk + lane * 32);
+                    uint4 o0, o1;
+                    o0.x = pack_bf16x2(acc[16 * c + 0], acc[16 * c + 1]);
+                    o0.y = pack_bf16x2(acc[16 * c + 2], acc[16 * c + 3]);
+                    o0.z = pack_bf16x2(acc[16 * c + 4], acc[16 * c + 5]);
+                    o0.w = pack_bf16x2(acc[16 * c + 6], acc[16 * c + 7]);
+                    o1.x = pack_bf16x2(acc[16 * c + 8], acc[16 * c + 9]);
+                    o1.y = pack_bf16x2(acc[16 * c + 10], acc[16 * c + 11]);
+                    o1.z = pack_bf16x2(acc[16 * c + 12], acc[16 * c + 13]);
+                    o1.w = pack_bf16x2(acc[16 * c + 14], acc[16 * c + 15]);
+                    dst[0] = o0;
+                    dst[1] = o1;
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        ptx::tma_store_2d(&tmap_d, chunk, col0 + 16 * c, tm * BM + quarter * 32);
+                        ptx::bulk_commit();
+                    }
                 }
             }
         }
+        if (lane == 0)
+            ptx::bulk_wait_all();                          // stores complete before the CTA exits
+        __syncwarp();
     }
 
     // ---------------------------------------------------------- teardown
@@ -418,7 +459,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
 
 template <int BN, int STAGES, bool SB_PER_COLUMN>
 cudaError_t launch_variant(const GemmProblem &p, const DeviceInfo &dev, const CUtensorMap &ta, const CUtensorMap &tb,
-                           cudaStream_t stream)
+                           const CUtensorMap &td, cudaStream_t stream)
 {
     using L = Smem<BN, STAGES>;
     auto kern = gemm_kernel<BN, STAGES, SB_PER_COLUMN>;
@@ -439,7 +480,7 @@ cudaError_t launch_variant(const GemmProblem &p, const DeviceInfo &dev, const CU
     a.tiles_n = static_cast<int32_t>((p.cols + BN - 1) / BN);
     const int tiles = a.tiles_m * a.tiles_n;
     const int grid = tiles < dev.sm_count ? tiles : dev.sm_count;
-    kern<<<grid, NUM_THREADS, L::TOTAL, stream>>>(ta, tb, a);
+    kern<<<grid, NUM_THREADS, L::TOTAL, stream>>>(ta, tb, td, a);
     return cudaGetLastError();
 }
 
@@ -455,6 +496,19 @@ CUresult encode_operand(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap *m
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+// bf16 output [rows][cols]: boxes of 32 rows x 16 columns (32-byte rows), no swizzle.
+CUresult encode_output(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap *map, void *ptr, int64_t rows,
+                       int64_t cols)
+{
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * 2)};
+    cuuint32_t box[2] = {16, 32};
+    cuuint32_t estr[2] = {1, 1};
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
 }  // namespace
 
 cudaError_t launch_gemm(const GemmProblem &p, const DeviceInfo &dev, PFN_cuTensorMapEncodeTiled_v12000 encode,
@@ -464,16 +518,17 @@ cudaError_t launch_gemm(const GemmProblem &p, const DeviceInfo &dev, PFN_cuTenso
     const int64_t tiles256 = ((p.rows + BM - 1) / BM) * ((p.cols + 255) / 256);
     const bool wide = tiles256 >= dev.sm_count;
     const int bn = wide ? 256 : 128;
-    CUtensorMap ta, tb;
+    CUtensorMap ta, tb, td;
     if (encode_operand(encode, &ta, p.a, p.rows, p.kdim, BM) != CUDA_SUCCESS ||
-        encode_operand(encode, &tb, p.b, p.cols, p.kdim, bn) != CUDA_SUCCESS)
+        encode_operand(encode, &tb, p.b, p.cols, p.kdim, bn) != CUDA_SUCCESS ||
+        encode_output(encode, &td, p.d, p.rows, p.cols) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     const bool per_col = p.sb_mode == ScaleB::PerColumn;
     if (wide)
-        return per_col ? launch_variant<256, 4, true>(p, dev, ta, tb, stream)
-                       : launch_variant<256, 4, false>(p, dev, ta, tb, stream);
-    return per_col ? launch_variant<128, 6, true>(p, dev, ta, tb, stream)
-                   : launch_variant<128, 6, false>(p, dev, ta, tb, stream);
+        return per_col ? launch_variant<256, 4, true>(p, dev, ta, tb, td, stream)
+                       : launch_variant<256, 4, false>(p, dev, ta, tb, td, stream);
+    return per_col ? launch_variant<128, 6, true>(p, dev, ta, tb, td, stream)
+                   : launch_variant<128, 6, false>(p, dev, ta, tb, td, stream);
 }
 
 // ---------------------------------------------------------------------------

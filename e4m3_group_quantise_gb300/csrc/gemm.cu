@@ -21,21 +21,17 @@
 //
 // Structure: persistent, one CTA per SM, 384 threads (3 warpgroups).
 //   warp 0, lane 0 : TMA producer   -- A and B tiles of one group per smem stage
-//   warp 1, lane 0 : MMA issuer     -- per group and per column half, 4 x
-//                                      tcgen05.mma (N = BN/2, K = 32 each) into
-//                                      one of four TMEM partial buffers
+//   warp 1, lane 0 : MMA issuer     -- 4 x tcgen05.mma (K = 32 each) per group
+//                                      into one of two TMEM partial buffers
 //   warp 2         : scale loader   -- cp.async of the group's row scales (128)
 //                                      and column scales into a smem ring
-//   warps 4..11    : promotion      -- two warpgroups, one per column half
-//                                      (128 rows x BN/2); tcgen05.ld the partial,
-//                                      free the buffer, acc += partial * sa * sb;
-//                                      bf16 epilogue: each warp stages 32 rows x
-//                                      16 columns in shared memory and TMA-stores
-//                                      them (double-buffered, asynchronous)
-// TMEM holds four BN/2-column partial buffers, two per half: the chain from an
-// MMA's completion through promotion's release to the next MMA into that
-// buffer (about 700 cycles measured) then overlaps three half-group MMAs
-// (768 cycles at BN = 256) instead of one.
+//   warps 4..11    : promotion      -- two warpgroups, each 128 rows x BN/2
+//                                      columns; tcgen05.ld the partial, free the
+//                                      buffer, acc += partial * sa * sb (packed
+//                                      fp32x2 FMAs); bf16 epilogue: each warp
+//                                      stages 32 rows x 16 columns in shared
+//                                      memory and TMA-stores them (double-
+//                                      buffered, asynchronous)
 // Registers are rebalanced with setmaxnreg: the control warpgroup drops to 40
 // per thread and the promotion warpgroups rise to 232 (128*40 + 256*232 =
 // 64512 = 384 threads * 168, the launch allocation).
@@ -94,8 +90,8 @@ struct Smem {
     static constexpr uint32_t OUT_CHUNK_BYTES = 32 * 16 * 2;
     static constexpr uint32_t OUT_BYTES = 8 * 2 * OUT_CHUNK_BYTES;
     static constexpr uint32_t BAR_OFF = OUT_OFF + OUT_BYTES;
-    // full[S], empty[S], sfull[SS], sempty[SS], tfull[4], tempty[4], mma_done, tmem holder, abort flag
-    static constexpr uint32_t CTRL_BYTES = (2 * STAGES + 2 * SCALE_STAGES + 9) * 8 + 16;
+    // full[S], empty[S], sfull[SS], sempty[SS], tfull[2], tempty[2], mma_done, tmem holder, abort flag
+    static constexpr uint32_t CTRL_BYTES = (2 * STAGES + 2 * SCALE_STAGES + 5) * 8 + 16;
     static constexpr uint32_t TOTAL = 1024 /* alignment slack */ + BAR_OFF + CTRL_BYTES;
 };
 
@@ -125,9 +121,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     constexpr int COLS_PER_WG = BN / 2;          // columns per promotion warpgroup
     constexpr int CHUNKS = COLS_PER_WG / 32;     // tcgen05.ld x32 per group
     static_assert(CHUNKS % 2 == 0, "loads are issued in pairs");
-    constexpr int HALF = BN / 2;                  // columns per MMA half = per TMEM buffer
-    constexpr uint32_t TMEM_COLS = 4 * HALF;     // four partial buffers
-    constexpr uint32_t IDESC = ptx::idesc_e4m3_f32(BM, HALF);
+    constexpr uint32_t TMEM_COLS = 2 * BN;       // two partial buffers
+    constexpr uint32_t IDESC = ptx::idesc_e4m3_f32(BM, BN);
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -139,8 +134,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     uint64_t *sfull = empty + STAGES;
     uint64_t *sempty = sfull + SCALE_STAGES;
     uint64_t *tfull = sempty + SCALE_STAGES;
-    uint64_t *tempty = tfull + 4;
-    uint64_t *mma_done = tempty + 4;
+    uint64_t *tempty = tfull + 2;
+    uint64_t *mma_done = tempty + 2;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(mma_done + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
 
@@ -159,9 +154,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                 ptx::mbar_init(&sfull[s], 32);   // every loader lane's copies
                 ptx::mbar_init(&sempty[s], 8);   // one arrival per promotion warp
             }
-            for (int b = 0; b < 4; ++b) {
+            for (int b = 0; b < 2; ++b) {
                 ptx::mbar_init(&tfull[b], 1);
-                ptx::mbar_init(&tempty[b], 4);   // one arrival per warp of the half's warpgroup
+                ptx::mbar_init(&tempty[b], 8);   // one arrival per promotion warp
             }
             ptx::mbar_init(mma_done, 1);
             *abort_flag = 0;
@@ -227,33 +222,24 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                 const uint32_t b_base = ptx::smem_u32(sB);
                 for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
                     for (int g = 0; g < G; ++g, ++it) {
+                        const uint32_t buf = it & 1u;
                         const uint32_t bphase = (it >> 1) & 1u;
-                        if (!ptx::mbar_wait(&full[stage], phase, abort_flag, args.err, ERRBIT_MMA_SMEM,
+                        if (!ptx::mbar_wait(&tempty[buf], bphase ^ 1u, abort_flag, args.err, ERRBIT_MMA_TMEM,
+                                            WAIT_TIMEOUT_NS) ||
+                            !ptx::mbar_wait(&full[stage], phase, abort_flag, args.err, ERRBIT_MMA_SMEM,
                                             WAIT_TIMEOUT_NS)) {
                             ok = false;
                             break;
                         }
+                        ptx::tc_fence_after();
                         const uint64_t adesc = ptx::smem_desc_sw128_kmajor(a_base + stage * L::A_BYTES);
+                        const uint64_t bdesc = ptx::smem_desc_sw128_kmajor(b_base + stage * L::B_BYTES);
+                        const uint32_t d_tmem = tmem_base + buf * BN;
 #pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const uint32_t buf = ((it & 1u) << 1) | h;
-                            if (!ptx::mbar_wait(&tempty[buf], bphase ^ 1u, abort_flag, args.err, ERRBIT_MMA_TMEM,
-                                                WAIT_TIMEOUT_NS)) {
-                                ok = false;
-                                break;
-                            }
-                            ptx::tc_fence_after();
-                            const uint64_t bdesc =
-                                ptx::smem_desc_sw128_kmajor(b_base + stage * L::B_BYTES + h * HALF * BK);
-                            const uint32_t d_tmem = tmem_base + buf * HALF;
-#pragma unroll
-                            for (int j = 0; j < BK / 32; ++j)   // 32 bytes of K per instruction: +2 in the >>4 field
-                                ptx::mma_f8(d_tmem, adesc + 2 * j, bdesc + 2 * j, IDESC, j > 0 ? 1u : 0u);
-                            ptx::mma_commit(&tfull[buf]);
-                        }
-                        if (!ok)
-                            break;
+                        for (int j = 0; j < BK / 32; ++j)   // 32 bytes of K per instruction: +2 in the >>4 field
+                            ptx::mma_f8(d_tmem, adesc + 2 * j, bdesc + 2 * j, IDESC, j > 0 ? 1u : 0u);
                         ptx::mma_commit(&empty[stage]);
+                        ptx::mma_commit(&tfull[buf]);
                         if (++stage == STAGES) {
                             stage = 0;
                             phase ^= 1u;
@@ -328,13 +314,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
             int tm, tn;
             tile_coords(tile, args.tiles_m, args.tiles_n, tm, tn);
             const int col0 = tn * BN + wg * COLS_PER_WG;
-            float acc[COLS_PER_WG];
+            uint64_t acc[COLS_PER_WG / 2];               // fp32 pairs: columns 2i, 2i+1
 #pragma unroll
-            for (int i = 0; i < COLS_PER_WG; ++i)
-                acc[i] = 0.0f;
+            for (int i = 0; i < COLS_PER_WG / 2; ++i)
+                acc[i] = 0ull;
 
             for (int g = 0; g < G; ++g, ++it) {
-                const uint32_t buf = ((it & 1u) << 1) | wg;
+                const uint32_t buf = it & 1u;
                 const uint32_t bphase = (it >> 1) & 1u;
                 if (!ptx::mbar_wait(&sfull[ss], sphase, abort_flag, args.err, ERRBIT_PROMOTE, WAIT_TIMEOUT_NS)) {
                     ok = false;
@@ -356,7 +342,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                     break;
                 }
                 ptx::tc_fence_after();
-                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + buf * HALF;
+                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + buf * BN +
+                                       wg * COLS_PER_WG;
                 // Two 32-column loads in flight per wait (64 columns), so each
                 // group pays the TMEM load latency only COLS_PER_WG / 64 times.
 #pragma unroll
@@ -373,32 +360,26 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                         if (lane == 0)
                             ptx::mbar_arrive(&tempty[buf]);
                     }
-                    float *a0 = acc + h * 64;
+                    uint64_t *a0 = acc + h * 32;
                     if (SB_PER_COLUMN) {
-                        const float4 *sbv = reinterpret_cast<const float4 *>(sbcol + h * 64);
+                        // acc += p * (sa * sb[col]), two columns per instruction
+                        const uint64_t sa2 = ptx::pack_f32x2(sa, sa);
+                        const uint64_t *sbv = reinterpret_cast<const uint64_t *>(sbcol + h * 64);
 #pragma unroll
-                        for (int v = 0; v < 8; ++v) {
-                            const float4 s4 = sbv[v];
-                            a0[4 * v + 0] = fmaf(__uint_as_float(p0[4 * v + 0]), sa * s4.x, a0[4 * v + 0]);
-                            a0[4 * v + 1] = fmaf(__uint_as_float(p0[4 * v + 1]), sa * s4.y, a0[4 * v + 1]);
-                            a0[4 * v + 2] = fmaf(__uint_as_float(p0[4 * v + 2]), sa * s4.z, a0[4 * v + 2]);
-                            a0[4 * v + 3] = fmaf(__uint_as_float(p0[4 * v + 3]), sa * s4.w, a0[4 * v + 3]);
-                        }
+                        for (int i = 0; i < 16; ++i)
+                            ptx::fma_f32x2(a0[i], ptx::pack_f32x2(p0[2 * i], p0[2 * i + 1]), ptx::mul_f32x2(sa2, sbv[i]));
 #pragma unroll
-                        for (int v = 0; v < 8; ++v) {
-                            const float4 s4 = sbv[8 + v];
-                            a0[32 + 4 * v + 0] = fmaf(__uint_as_float(p1[4 * v + 0]), sa * s4.x, a0[32 + 4 * v + 0]);
-                            a0[32 + 4 * v + 1] = fmaf(__uint_as_float(p1[4 * v + 1]), sa * s4.y, a0[32 + 4 * v + 1]);
-                            a0[32 + 4 * v + 2] = fmaf(__uint_as_float(p1[4 * v + 2]), sa * s4.z, a0[32 + 4 * v + 2]);
-                            a0[32 + 4 * v + 3] = fmaf(__uint_as_float(p1[4 * v + 3]), sa * s4.w, a0[32 + 4 * v + 3]);
-                        }
+                        for (int i = 0; i < 16; ++i)
+                            ptx::fma_f32x2(a0[16 + i], ptx::pack_f32x2(p1[2 * i], p1[2 * i + 1]),
+                                           ptx::mul_f32x2(sa2, sbv[16 + i]));
                     } else {
+                        const uint64_t w2 = ptx::pack_f32x2(w_blk, w_blk);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            a0[i] = fmaf(__uint_as_float(p0[i]), w_blk, a0[i]);
+                        for (int i = 0; i < 16; ++i)
+                            ptx::fma_f32x2(a0[i], ptx::pack_f32x2(p0[2 * i], p0[2 * i + 1]), w2);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            a0[32 + i] = fmaf(__uint_as_float(p1[i]), w_blk, a0[32 + i]);
+                        for (int i = 0; i < 16; ++i)
+                            ptx::fma_f32x2(a0[16 + i], ptx::pack_f32x2(p1[2 * i], p1[2 * i + 1]), w2);
                     }
                 }
                 if (SB_PER_COLUMN) {
@@ -425,14 +406,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                     __syncwarp();
                     uint4 *dst = reinterpret_cast<uint4 *>(chunk + lane * 32);
                     uint4 o0, o1;
-                    o0.x = pack_bf16x2(acc[16 * c + 0], acc[16 * c + 1]);
-                    o0.y = pack_bf16x2(acc[16 * c + 2], acc[16 * c + 3]);
-                    o0.z = pack_bf16x2(acc[16 * c + 4], acc[16 * c + 5]);
-                    o0.w = pack_bf16x2(acc[16 * c + 6], acc[16 * c + 7]);
-                    o1.x = pack_bf16x2(acc[16 * c + 8], acc[16 * c + 9]);
-                    o1.y = pack_bf16x2(acc[16 * c + 10], acc[16 * c + 11]);
-                    o1.z = pack_bf16x2(acc[16 * c + 12], acc[16 * c + 13]);
-                    o1.w = pack_bf16x2(acc[16 * c + 14], acc[16 * c + 15]);
+                    const uint64_t *ac = acc + 8 * c;
+                    o0.x = pack_bf16x2(ptx::lo_f32(ac[0]), ptx::hi_f32(ac[0]));
+                    o0.y = pack_bf16x2(ptx::lo_f32(ac[1]), ptx::hi_f32(ac[1]));
+                    o0.z = pack_bf16x2(ptx::lo_f32(ac[2]), ptx::hi_f32(ac[2]));
+                    o0.w = pack_bf16x2(ptx::lo_f32(ac[3]), ptx::hi_f32(ac[3]));
+                    o1.x = pack_bf16x2(ptx::lo_f32(ac[4]), ptx::hi_f32(ac[4]));
+                    o1.y = pack_bf16x2(ptx::lo_f32(ac[5]), ptx::hi_f32(ac[5]));
+                    o1.z = pack_bf16x2(ptx::lo_f32(ac[6]), ptx::hi_f32(ac[6]));
+                    o1.w = pack_bf16x2(ptx::lo_f32(ac[7]), ptx::hi_f32(ac[7]));
                     dst[0] = o0;
                     dst[1] = o1;
                     ptx::fence_proxy_async_smem();

@@ -309,6 +309,37 @@ __device__ __forceinline__ void setmaxnreg_dec()
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
+// ------------------------------------------------------------ packed fp32
+// Two fp32 lanes in one 64-bit register (lo in bits 0..31).  The f32x2 forms
+// round each half exactly like their scalar counterparts.
+__device__ __forceinline__ uint64_t pack_f32x2(uint32_t lo, uint32_t hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+    return r;
+}
+
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi)
+{
+    return pack_f32x2(__float_as_uint(lo), __float_as_uint(hi));
+}
+
+__device__ __forceinline__ float lo_f32(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v)); }
+__device__ __forceinline__ float hi_f32(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v >> 32)); }
+
+// acc = p * w + acc, lane-wise
+__device__ __forceinline__ void fma_f32x2(uint64_t &acc, uint64_t p, uint64_t w)
+{
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(p), "l"(w));
+}
+
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
 // ------------------------------------------------------------ convert
 // Two fp32 -> two E4M3 codes, round to nearest even, saturating to +-448.
 // Returns lo's code in bits 0..7 and hi's code in bits 8..15.

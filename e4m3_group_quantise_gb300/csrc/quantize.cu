@@ -181,67 +181,72 @@ quantize_act_kernel(const uint4 *__restrict__ x, int64_t M, int64_t K, uint2 *__
 
 // ---------------------------------------------------------------------------
 // 128x1 groups along rows (tokens) of each column, written transposed.
-// CTA tile: 128 rows x 64 columns of bf16 staged in shared memory (16-byte
-// chunks XOR-swizzled by row so that both the row-wise fill and the
-// column-wise reads are bank-conflict free).  Warp w reads column
-// 32*(w&1)+lane over rows 32*(w>>1) .. +31; the four row quarters combine
+// CTA tile: 128 rows x 64 columns of bf16 staged in shared memory (128 bytes
+// per row).  Warp q takes rows 32q .. 32q+31; lane l takes the column pair
+// 2l, 2l+1, reading one 4-byte word per row (a warp reads one contiguous
+// 128-byte row per step: no bank conflicts).  The four row quarters combine
 // their amax through shared memory; each thread then writes 32 contiguous
-// codes (one full 32-byte sector) of its output row.
+// codes (one 32-byte sector) to each of its two output rows.
 // ---------------------------------------------------------------------------
 constexpr int Q2_ROWS = 128;
 constexpr int Q2_COLS = 64;
-constexpr int Q2_THREADS = 256;
+constexpr int Q2_THREADS = 128;
 
 __global__ void __launch_bounds__(Q2_THREADS)
 quantize_act_t_kernel(const uint4 *__restrict__ x, int64_t M, int64_t C, uint8_t *__restrict__ qt,
                       float *__restrict__ st)
 {
     __shared__ uint4 tile[Q2_ROWS][Q2_COLS / 8];
-    __shared__ float s_amax[4][Q2_COLS];
-    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    __shared__ float2 s_amax[4][Q2_COLS / 2];
+    const int t = threadIdx.x, q = t >> 5, lane = t & 31;
     const int64_t m0 = static_cast<int64_t>(blockIdx.x) * Q2_ROWS;
     const int64_t c0 = static_cast<int64_t>(blockIdx.y) * Q2_COLS;
     const int64_t C8 = C >> 3;
 
-    uint4 v[4];
+    uint4 v[8];
 #pragma unroll
-    for (int p = 0; p < 4; ++p) {
+    for (int p = 0; p < 8; ++p) {
         const int idx = p * Q2_THREADS + t;
-        const int r = idx >> 3, ch = idx & 7;
-        v[p] = __ldcs(x + (m0 + r) * C8 + (c0 >> 3) + ch);
+        v[p] = __ldcs(x + (m0 + (idx >> 3)) * C8 + (c0 >> 3) + (idx & 7));
     }
 #pragma unroll
-    for (int p = 0; p < 4; ++p) {
+    for (int p = 0; p < 8; ++p) {
         const int idx = p * Q2_THREADS + t;
-        const int r = idx >> 3, ch = idx & 7;
-        tile[r][ch ^ (r & 7)] = v[p];
+        tile[idx >> 3][idx & 7] = v[p];
     }
     __syncthreads();
 
-    const int c = 32 * (warp & 1) + lane;   // column within the tile
-    const int qd = warp >> 1;               // row quarter
-    const int chunk = c >> 3, elem = c & 7;
-    float f[32];
-    float amax = 0.0f;
+    float f0[32], f1[32];
+    float a0 = 0.0f, a1 = 0.0f;
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-        const int r = 32 * qd + i;
-        const uint16_t *row = reinterpret_cast<const uint16_t *>(&tile[r][0]);
-        f[i] = __uint_as_float(static_cast<uint32_t>(row[((chunk ^ (r & 7)) << 3) + elem]) << 16);
-        amax = fmaxf(amax, fabsf(f[i]));
+        const uint32_t w = reinterpret_cast<const uint32_t *>(&tile[32 * q + i][0])[lane];
+        f0[i] = bf16_lo(w);
+        f1[i] = bf16_hi(w);
+        a0 = fmaxf(a0, fabsf(f0[i]));
+        a1 = fmaxf(a1, fabsf(f1[i]));
     }
-    s_amax[qd][c] = amax;
+    s_amax[q][lane] = make_float2(a0, a1);
     __syncthreads();
-    amax = fmaxf(fmaxf(s_amax[0][c], s_amax[1][c]), fmaxf(s_amax[2][c], s_amax[3][c]));
-    const GroupScale gs = group_scale(amax);
-
-    uint32_t w[8];
-    encode_run<32>(f, gs, w);
-    uint4 *dst = reinterpret_cast<uint4 *>(qt + (c0 + c) * M + m0 + 32 * qd);
-    __stcs(dst, make_uint4(w[0], w[1], w[2], w[3]));
-    __stcs(dst + 1, make_uint4(w[4], w[5], w[6], w[7]));
-    if (qd == 0)
-        st[(m0 >> 7) * C + c0 + c] = gs.s;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float2 o = s_amax[k][lane];
+        a0 = fmaxf(a0, o.x);
+        a1 = fmaxf(a1, o.y);
+    }
+    const GroupScale g0 = group_scale(a0), g1 = group_scale(a1);
+    uint32_t w0[8], w1[8];
+    encode_run<32>(f0, g0, w0);
+    encode_run<32>(f1, g1, w1);
+    const int64_t col = c0 + 2 * lane;
+    uint4 *d0 = reinterpret_cast<uint4 *>(qt + col * M + m0 + 32 * q);
+    uint4 *d1 = reinterpret_cast<uint4 *>(qt + (col + 1) * M + m0 + 32 * q);
+    __stcs(d0, make_uint4(w0[0], w0[1], w0[2], w0[3]));
+    __stcs(d0 + 1, make_uint4(w0[4], w0[5], w0[6], w0[7]));
+    __stcs(d1, make_uint4(w1[0], w1[1], w1[2], w1[3]));
+    __stcs(d1 + 1, make_uint4(w1[4], w1[5], w1[6], w1[7]));
+    if (q == 0)
+        *reinterpret_cast<float2 *>(st + (m0 >> 7) * C + col) = make_float2(g0.s, g1.s);
 }
 
 // ---------------------------------------------------------------------------

@@ -45,34 +45,39 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+// One potentially blocking test of the phase with parity `parity`: the thread
+// is suspended (issuing nothing) until the phase completes or about
+// `suspend_ns` nanoseconds pass, whichever is first.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity, uint32_t suspend_ns)
 {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(suspend_ns)
         : "memory");
     return ok != 0;
 }
 
 // Bounded wait for the phase of `bar` with parity `parity` to complete.
+// Waiting threads sleep inside try_wait (so they take no issue slots from the
+// warps that share their SM sub-partition) and wake when the phase completes.
 // Gives up (returns false) when *abort becomes non-zero (another role gave
 // up) or after timeout_ns; on a timeout it sets *abort and ORs `code` into
 // the device error word so the host can see what happened.
+constexpr uint32_t SUSPEND_NS = 200000;   // re-check abort / timeout every 0.2 ms at most
+
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
                                           uint32_t *err_word, uint32_t code, uint64_t timeout_ns)
 {
-    if (mbar_try_wait(bar, parity))
+    if (mbar_try_wait(bar, parity, SUSPEND_NS))
         return true;
     const uint64_t t0 = globaltimer();
     while (true) {
-#pragma unroll 1
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(bar, parity))
-                return true;
+        if (mbar_try_wait(bar, parity, SUSPEND_NS))
+            return true;
         if (abort != nullptr && *abort)
             return false;
         if (globaltimer() - t0 > timeout_ns) {

@@ -5,6 +5,8 @@ A step runs every stage of the path for each projection (QKV 6144x4096,
 O 4096x4096, gate_up 28672x4096, down 4096x14336; M = 16384 tokens = 8 x 2048):
   quantise W (128x128 blocks, + transposed codes), quantise X (1x128) and
   X^T (128x1), quantise dY (1x128) and dY^T (128x1), then Fprop, Dgrad, Wgrad.
+The two layouts of X (and of dY) come from one dual-output quantiser launch
+each, as the training path (FP8Linear) produces them.
 Metric: block-scaled FP8 GEMM TFLOP/s = (Fprop + Dgrad + Wgrad FLOPs, 2MNK
 each) / step time, the step time including the quantisers.  Inputs are
 synthetic (seeded) and resident in HBM; the step's working set (~8 GB) is far
@@ -36,12 +38,13 @@ sys.path.insert(0, ROOT)
 METRIC = "block-scaled FP8 GEMM TFLOP/s (fprop/dgrad/wgrad), % of GB300 FP8 peak"
 TOKENS = 16384
 PROJ = {"qkv": (6144, 4096), "o": (4096, 4096), "gate_up": (28672, 4096), "down": (4096, 14336)}
-WORKLOAD = ("train-8b: full FP8 training step (quantise W, X, X^T, dY, dY^T; fprop, dgrad, wgrad) on the "
+WORKLOAD = ("train-8b: full FP8 training step (quantise W; quantise X and X^T, dY and dY^T with the dual-output "
+            "quantiser; fprop, dgrad, wgrad) on the "
             "four 8B-class projections qkv 6144x4096, o 4096x4096, gate_up 28672x4096, down 4096x14336 "
             "at M=16384 tokens (8 x 2048)")
 FP8_PER_BF16 = 4.5 / 2.25          # nominal dense fp8 : bf16 tensor ratio
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNELS = ("quant_w", "quant_x", "quant_xt", "quant_dy", "quant_dyt", "fprop", "dgrad", "wgrad")
+KERNELS = ("quant_w", "quant_x_dual", "quant_dy_dual", "fprop", "dgrad", "wgrad")
 
 
 def gemm_flops() -> float:
@@ -52,8 +55,10 @@ def quant_bytes(kind: str, n: int, k: int) -> float:
     """Algorithmic bytes of one quantiser launch."""
     if kind == "quant_w":                      # read bf16, write codes + transposed codes + scales
         return n * k * (2 + 1 + 1) + 4 * (n // 128) * (k // 128)
-    rows, cols = {"quant_x": (TOKENS, k), "quant_xt": (TOKENS, k),
-                  "quant_dy": (TOKENS, n), "quant_dyt": (TOKENS, n)}[kind]
+    rows, cols = {"quant_x": (TOKENS, k), "quant_xt": (TOKENS, k), "quant_x_dual": (TOKENS, k),
+                  "quant_dy": (TOKENS, n), "quant_dyt": (TOKENS, n), "quant_dy_dual": (TOKENS, n)}[kind]
+    if kind.endswith("_dual"):                 # read bf16 once, write both code layouts and scales
+        return rows * cols * (2 + 2 + 8 / 128)
     return rows * cols * (2 + 1 + 4 / 128)
 
 
@@ -144,10 +149,9 @@ class Step:
         jf = self.jf
         return (
             ("quant_w", lambda: jf.jetfp8_quantize_weight(d["w"], d["qw"], d["sw"], d["qwt"])),
-            ("quant_x", lambda: jf.jetfp8_quantize_act(d["x"], d["qx"], d["sx"])),
-            ("quant_xt", lambda: jf.jetfp8_quantize_act_transposed(d["x"], d["qxt"], d["sxt"])),
-            ("quant_dy", lambda: jf.jetfp8_quantize_act(d["dy"], d["qdy"], d["sdy"])),
-            ("quant_dyt", lambda: jf.jetfp8_quantize_act_transposed(d["dy"], d["qdyt"], d["sdyt"])),
+            ("quant_x_dual", lambda: jf.jetfp8_quantize_act_dual(d["x"], d["qx"], d["sx"], d["qxt"], d["sxt"])),
+            ("quant_dy_dual", lambda: jf.jetfp8_quantize_act_dual(d["dy"], d["qdy"], d["sdy"], d["qdyt"],
+                                                                  d["sdyt"])),
             ("fprop", lambda: jf.jetfp8_gemm_fprop(d["qx"], d["sx"], d["qw"], d["sw"], d["y"])),
             ("dgrad", lambda: jf.jetfp8_gemm_dgrad(d["qdy"], d["sdy"], d["qwt"], d["sw"], d["dx"])),
             ("wgrad", lambda: jf.jetfp8_gemm_wgrad(d["qdyt"], d["sdyt"], d["qxt"], d["sxt"], d["dw"])),
@@ -294,7 +298,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
     ap.add_argument("--case", default=None,
                     help="time one kernel alone, e.g. fprop:16384x6144x4096 (KIND:MxNxK; KIND in fprop, dgrad, "
-                         "wgrad, quant_x, quant_xt, quant_w) -- a single-kernel line for profiling, not the metric")
+                         "wgrad, quant_x, quant_xt, quant_dual, quant_w) -- a single-kernel line for profiling, not the metric")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -392,9 +396,13 @@ def run_case(args):
         qdyt, sdyt = jf.quantize_act_transposed(syn.grad_output(M, N, seed=1, device=dev))
         out = torch.empty(N, K, dtype=torch.bfloat16, device=dev)
         fn = lambda: jf.jetfp8_gemm_wgrad(qdyt, sdyt, qxt, sxt, out)  # noqa: E731
-    elif kind in ("quant_x", "quant_xt"):
+    elif kind in ("quant_x", "quant_xt", "quant_dual"):
         x = syn.activation(M, K, seed=1, device=dev, outlier_scale=20.0)
-        if kind == "quant_x":
+        if kind == "quant_dual":
+            q, s = torch.empty(M, K, dtype=torch.uint8, device=dev), torch.empty(K // 128, M, device=dev)
+            qt, st = torch.empty(K, M, dtype=torch.uint8, device=dev), torch.empty(M // 128, K, device=dev)
+            fn = lambda: jf.jetfp8_quantize_act_dual(x, q, s, qt, st)  # noqa: E731
+        elif kind == "quant_x":
             q, s = torch.empty(M, K, dtype=torch.uint8, device=dev), torch.empty(K // 128, M, device=dev)
             fn = lambda: jf.jetfp8_quantize_act(x, q, s)  # noqa: E731
         else:
@@ -422,7 +430,12 @@ def run_case(args):
     if kind in ("fprop", "dgrad", "wgrad"):
         rec["tflops"] = round(2.0 * M * N * K / (ms * 1e-3) / 1e12, 1)
     else:
-        byts = N * K * 4 + 4 * (N // 128) * (K // 128) if kind == "quant_w" else M * K * (3 + 4 / 128)
+        if kind == "quant_w":
+            byts = N * K * 4 + 4 * (N // 128) * (K // 128)
+        elif kind == "quant_dual":
+            byts = M * K * (4 + 8 / 128)
+        else:
+            byts = M * K * (3 + 4 / 128)
         rec["gbs"] = round(byts / (ms * 1e-3) / 1e9, 1)
     assert jf.jetfp8_poll_device_error() == 0
     print(json.dumps(rec))

@@ -13,12 +13,14 @@ from .jetfp8 import (  # noqa: F401
     jetfp8_gemm_wgrad,
     jetfp8_poll_device_error,
     jetfp8_quantize_act,
+    jetfp8_quantize_act_dual,
     jetfp8_quantize_act_transposed,
     jetfp8_quantize_weight,
     jetfp8_status_string,
     jetfp8_watchdog_selftest,
     load_library,
     quantize_act,
+    quantize_act_dual,
     quantize_act_transposed,
     quantize_weight,
 )

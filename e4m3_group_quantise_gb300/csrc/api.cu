@@ -212,6 +212,29 @@ JETFP8_API jetfp8_status jetfp8_quantize_act_transposed(const void *x, int64_t M
         jetfp8::launch_quantize_act_transposed(x, M, C, qt, st, static_cast<cudaStream_t>(stream)));
 }
 
+JETFP8_API jetfp8_status jetfp8_quantize_act_dual(const void *x, int64_t M, int64_t K, uint8_t *q, float *s,
+                                                  uint8_t *qt, float *st, void *stream)
+{
+    if (M < 0 || M % 128 != 0 || K <= 0 || K % 128 != 0 || !dims_ok(M, K) || K / 128 > 65535)
+        return JETFP8_ERR_SHAPE;
+    if (M == 0)
+        return JETFP8_OK;
+    if (!x || !q || !s || !qt || !st)
+        return JETFP8_ERR_INVALID_VALUE;
+    if (!aligned16(x) || !aligned16(q) || !aligned16(s) || !aligned16(qt) || !aligned16(st))
+        return JETFP8_ERR_ALIGNMENT;
+    const Range outs[4] = {range_of(q, M * K), range_of(s, M * (K / 128) * 4), range_of(qt, M * K),
+                           range_of(st, (M / 128) * K * 4)};
+    const Range ins[1] = {range_of(x, M * K * 2)};
+    if (any_overlap(outs, 4, ins, 1))
+        return JETFP8_ERR_INVALID_VALUE;
+    const DeviceInfo *dev = nullptr;
+    jetfp8_status status = current_device(&dev);
+    if (status != JETFP8_OK)
+        return status;
+    return launch_status(jetfp8::launch_quantize_act_dual(x, M, K, q, s, qt, st, static_cast<cudaStream_t>(stream)));
+}
+
 JETFP8_API jetfp8_status jetfp8_quantize_weight(const void *w, int64_t N, int64_t K, uint8_t *q, float *s,
                                                 uint8_t *qt, void *stream)
 {

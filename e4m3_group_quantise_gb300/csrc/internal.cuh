@@ -24,6 +24,8 @@ cudaError_t launch_quantize_act(const void *x, int64_t M, int64_t K, uint8_t *q,
                                 cudaStream_t stream);
 cudaError_t launch_quantize_act_transposed(const void *x, int64_t M, int64_t C, uint8_t *qt, float *st,
                                            cudaStream_t stream);
+cudaError_t launch_quantize_act_dual(const void *x, int64_t M, int64_t K, uint8_t *q, float *s, uint8_t *qt,
+                                     float *st, cudaStream_t stream);
 cudaError_t launch_quantize_weight(const void *w, int64_t N, int64_t K, uint8_t *q, float *s, uint8_t *qt,
                                    cudaStream_t stream);
 

@@ -325,6 +325,118 @@ quantize_weight_kernel(const uint4 *__restrict__ w, int64_t N, int64_t K, uint2 
         __stcs(dst + i, make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]));
 }
 
+// ---------------------------------------------------------------------------
+// Dual output: one read of X [M][K] yields both the 1x128 row-group codes and
+// scales (as quantize_act_kernel) and the 128x1 column-group codes and scales
+// written transposed (as quantize_act_t_kernel).  CTA tile: 128 rows x 128
+// columns of bf16 in shared memory, 16-byte chunks XOR-swizzled by
+// (row & 15) so that both read patterns below are bank-conflict free.
+//   rows:    thread (r = t % 128, half h = t / 128) reads 64 values of row r;
+//            the two halves combine their amax through shared memory; each
+//            thread writes 64 contiguous codes; h == 0 writes the row's scale.
+//   columns: warp w covers rows 32*(w>>1) .. +31 and column pairs
+//            32*(w&1) + lane; the four row quarters combine their amax through
+//            shared memory; each thread writes 32 contiguous codes per column.
+// The arithmetic of every group is exactly that of the single-output kernels.
+// ---------------------------------------------------------------------------
+constexpr int QD_TILE = 128;
+constexpr int QD_THREADS = 256;
+
+__global__ void __launch_bounds__(QD_THREADS)
+quantize_act_dual_kernel(const uint4 *__restrict__ x, int64_t M, int64_t K, uint8_t *__restrict__ q,
+                         float *__restrict__ s, uint8_t *__restrict__ qt, float *__restrict__ st)
+{
+    __shared__ uint4 tile[QD_TILE][QD_TILE / 8];
+    __shared__ float s_ramax[2][QD_TILE];
+    __shared__ float2 s_camax[4][QD_TILE / 2];
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const int64_t m0 = static_cast<int64_t>(blockIdx.x) * QD_TILE;
+    const int64_t k0 = static_cast<int64_t>(blockIdx.y) * QD_TILE;
+    const int64_t K8 = K >> 3;
+
+    uint4 v[8];
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+        const int idx = p * QD_THREADS + t;          // 16 chunks per row
+        v[p] = __ldcs(x + (m0 + (idx >> 4)) * K8 + (k0 >> 3) + (idx & 15));
+    }
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+        const int idx = p * QD_THREADS + t;
+        const int r = idx >> 4, c = idx & 15;
+        tile[r][c ^ (r & 15)] = v[p];
+    }
+    __syncthreads();
+
+    // ---- 1x128 groups along rows -----------------------------------------
+    {
+        const int r = t & 127, h = t >> 7;
+        float f[64];
+        float amax = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            float u[8];
+            unpack8(tile[r][(8 * h + j) ^ (r & 15)], u);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                f[8 * j + e] = u[e];
+                amax = fmaxf(amax, fabsf(u[e]));
+            }
+        }
+        s_ramax[h][r] = amax;
+        __syncthreads();
+        amax = fmaxf(s_ramax[0][r], s_ramax[1][r]);
+        const GroupScale gs = group_scale(amax);
+        uint32_t w[16];
+        encode_run<64>(f, gs, w);
+        uint4 *dst = reinterpret_cast<uint4 *>(q + (m0 + r) * K + k0 + 64 * h);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            __stcs(dst + j, make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]));
+        if (h == 0)
+            s[(k0 >> 7) * M + m0 + r] = gs.s;
+    }
+
+    // ---- 128x1 groups along columns, written transposed -------------------
+    {
+        const int qd = warp >> 1;                   // row quarter
+        const int p = 32 * (warp & 1) + lane;       // column pair
+        float f0[32], f1[32];
+        float a0 = 0.0f, a1 = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const int r = 32 * qd + i;
+            const uint32_t *row = reinterpret_cast<const uint32_t *>(&tile[r][0]);
+            const uint32_t wv = row[(((p >> 2) ^ (r & 15)) << 2) + (p & 3)];
+            f0[i] = bf16_lo(wv);
+            f1[i] = bf16_hi(wv);
+            a0 = fmaxf(a0, fabsf(f0[i]));
+            a1 = fmaxf(a1, fabsf(f1[i]));
+        }
+        s_camax[qd][p] = make_float2(a0, a1);
+        __syncthreads();
+#pragma unroll
+        for (int kq = 0; kq < 4; ++kq) {
+            const float2 o = s_camax[kq][p];
+            a0 = fmaxf(a0, o.x);
+            a1 = fmaxf(a1, o.y);
+        }
+        const GroupScale g0 = group_scale(a0), g1 = group_scale(a1);
+        uint32_t w0[8], w1[8];
+        encode_run<32>(f0, g0, w0);
+        encode_run<32>(f1, g1, w1);
+        const int64_t col = k0 + 2 * p;
+        uint4 *d0 = reinterpret_cast<uint4 *>(qt + col * M + m0 + 32 * qd);
+        uint4 *d1 = reinterpret_cast<uint4 *>(qt + (col + 1) * M + m0 + 32 * qd);
+        __stcs(d0, make_uint4(w0[0], w0[1], w0[2], w0[3]));
+        __stcs(d0 + 1, make_uint4(w0[4], w0[5], w0[6], w0[7]));
+        __stcs(d1, make_uint4(w1[0], w1[1], w1[2], w1[3]));
+        __stcs(d1 + 1, make_uint4(w1[4], w1[5], w1[6], w1[7]));
+        if (qd == 0)
+            *reinterpret_cast<float2 *>(st + (m0 >> 7) * K + col) = make_float2(g0.s, g1.s);
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_quantize_act(const void *x, int64_t M, int64_t K, uint8_t *q, float *s, cudaStream_t stream)
@@ -354,4 +466,14 @@ cudaError_t launch_quantize_weight(const void *w, int64_t N, int64_t K, uint8_t 
     return cudaGetLastError();
 }
 
+}  // namespace jetfp8
+
+namespace jetfp8 {
+cudaError_t launch_quantize_act_dual(const void *x, int64_t M, int64_t K, uint8_t *q, float *s, uint8_t *qt,
+                                     float *st, cudaStream_t stream)
+{
+    dim3 grid(static_cast<unsigned>(M / QD_TILE), static_cast<unsigned>(K / QD_TILE));
+    quantize_act_dual_kernel<<<grid, QD_THREADS, 0, stream>>>(static_cast<const uint4 *>(x), M, K, q, s, qt, st);
+    return cudaGetLastError();
+}
 }  // namespace jetfp8

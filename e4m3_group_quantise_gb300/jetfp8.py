@@ -59,9 +59,11 @@ def load_library():
     lib.jetfp8_quantize_act.argtypes = [P, I, I, P, P, P]
     lib.jetfp8_quantize_act_transposed.argtypes = [P, I, I, P, P, P]
     lib.jetfp8_quantize_weight.argtypes = [P, I, I, P, P, P, P]
+    lib.jetfp8_quantize_act_dual.argtypes = [P, I, I, P, P, P, P, P]
     for name in ("jetfp8_gemm_fprop", "jetfp8_gemm_dgrad", "jetfp8_gemm_wgrad"):
         getattr(lib, name).argtypes = [P, P, P, P, P, I, I, I, P]
     for name in ("jetfp8_quantize_act", "jetfp8_quantize_act_transposed", "jetfp8_quantize_weight",
+                 "jetfp8_quantize_act_dual",
                  "jetfp8_gemm_fprop", "jetfp8_gemm_dgrad", "jetfp8_gemm_wgrad"):
         getattr(lib, name).restype = S
     lib.jetfp8_act_scale_count.argtypes = [I, I]
@@ -134,6 +136,17 @@ def jetfp8_quantize_act_transposed(x, qt, st, stream=None):
     _want(st, torch.float32, (M // 128, C), "st")
     _check(load_library().jetfp8_quantize_act_transposed(_ptr(x), M, C, _ptr(qt), _ptr(st), _stream(stream)),
            "jetfp8_quantize_act_transposed")
+
+
+def jetfp8_quantize_act_dual(x, q, s, qt, st, stream=None):
+    M, K = x.shape
+    _want(x, torch.bfloat16, (M, K), "x")
+    _want(q, torch.uint8, (M, K), "q")
+    _want(s, torch.float32, (K // 128, M), "s")
+    _want(qt, torch.uint8, (K, M), "qt")
+    _want(st, torch.float32, (M // 128, K), "st")
+    _check(load_library().jetfp8_quantize_act_dual(_ptr(x), M, K, _ptr(q), _ptr(s), _ptr(qt), _ptr(st),
+                                                   _stream(stream)), "jetfp8_quantize_act_dual")
 
 
 def jetfp8_quantize_weight(w, q, s, qt=None, stream=None):
@@ -217,6 +230,17 @@ def quantize_act_transposed(x: torch.Tensor, stream=None):
     st = torch.empty((M // 128, C), dtype=torch.float32, device=x.device)
     jetfp8_quantize_act_transposed(x, qt, st, stream)
     return qt, st
+
+
+def quantize_act_dual(x: torch.Tensor, stream=None):
+    """bf16 [M,K] -> (q [M,K], s [K/128,M], qt [K,M], st [M/128,K]) in one pass."""
+    M, K = x.shape
+    q = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    s = torch.empty((K // 128, M), dtype=torch.float32, device=x.device)
+    qt = torch.empty((K, M), dtype=torch.uint8, device=x.device)
+    st = torch.empty((M // 128, K), dtype=torch.float32, device=x.device)
+    jetfp8_quantize_act_dual(x, q, s, qt, st, stream)
+    return q, s, qt, st
 
 
 def quantize_weight(w: torch.Tensor, transposed: bool = True, stream=None):

@@ -44,12 +44,14 @@ class FP8LinearFunction(torch.autograd.Function):
     @staticmethod
     def forward(ctx, x2d: torch.Tensor, weight: torch.Tensor, cache: QuantizedWeight):
         q, s, qt = cache.get(weight)
-        qx, sx = _j.quantize_act(x2d)
-        y = _j.gemm_fprop(qx, sx, q, s)
         if ctx.needs_input_grad[1]:
-            qxt, sxt = _j.quantize_act_transposed(x2d)     # saved activation, FP8
+            # one read of X: 1x128 codes for Fprop + the transposed 128x1 codes
+            # saved (in FP8) for Wgrad; the former are bit-identical to rollout's
+            qx, sx, qxt, sxt = _j.quantize_act_dual(x2d)
         else:
+            qx, sx = _j.quantize_act(x2d)
             qxt = sxt = None
+        y = _j.gemm_fprop(qx, sx, q, s)
         ctx.save_for_backward(qt, s, qxt, sxt)
         return y
 
@@ -58,11 +60,15 @@ class FP8LinearFunction(torch.autograd.Function):
         qt, s, qxt, sxt = ctx.saved_tensors
         dy = dy.contiguous()
         dx = dw = None
-        if ctx.needs_input_grad[0]:
+        if ctx.needs_input_grad[0] and ctx.needs_input_grad[1]:
+            qdy, sdy, qdyt, sdyt = _j.quantize_act_dual(dy)
+        elif ctx.needs_input_grad[0]:
             qdy, sdy = _j.quantize_act(dy)
+        elif ctx.needs_input_grad[1]:
+            qdyt, sdyt = _j.quantize_act_transposed(dy)
+        if ctx.needs_input_grad[0]:
             dx = _j.gemm_dgrad(qdy, sdy, qt, s)
         if ctx.needs_input_grad[1]:
-            qdyt, sdyt = _j.quantize_act_transposed(dy)
             dw = _j.gemm_wgrad(qdyt, sdyt, qxt, sxt)
         return dx, dw, None
 

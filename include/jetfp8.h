@@ -98,6 +98,23 @@ JETFP8_API jetfp8_status jetfp8_quantize_act_transposed(const void *x, int64_t M
                                                         uint8_t *qt, float *st, void *stream);
 
 /*
+ * Both activation layouts from one read of x: exactly the outputs of
+ * jetfp8_quantize_act(x -> q, s) and jetfp8_quantize_act_transposed(x -> qt,
+ * st), bit for bit, at the HBM cost of reading x once.  This is the training
+ * forward's quantisation of X (the 1x128 codes feed Fprop, the transposed
+ * 128x1 codes are the activation saved in FP8 for WGrad) and the backward's
+ * quantisation of dY (DGrad and WGrad operands) -- Jet-RL, "Schéma de
+ * Quantification": saved activations kept in FP8; "Implémentation": fused
+ * quantisation and transposition kernels.
+ *   x  : bf16 [M][K]
+ *   q  : uint8 [M][K],  s  : fp32 [K/128][M]   (as jetfp8_quantize_act)
+ *   qt : uint8 [K][M],  st : fp32 [M/128][K]   (as jetfp8_quantize_act_transposed)
+ * Requires M % 128 == 0, K > 0, K % 128 == 0, M * K < 2^40.
+ */
+JETFP8_API jetfp8_status jetfp8_quantize_act_dual(const void *x, int64_t M, int64_t K, uint8_t *q, float *s,
+                                                  uint8_t *qt, float *st, void *stream);
+
+/*
  * Weight quantisation, 128x128 blocks (Jet-RL, "Schéma de Quantification":
  * weights 128x128 per block; master weights stay BF16, "Architecture
  * Centrale").

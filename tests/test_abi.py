@@ -72,6 +72,16 @@ def test_quantize_transposed_validation(lib):
     assert f(A16, 128, 128, A16 + 16, C16, None) == J.ERR_INVALID_VALUE
 
 
+def test_quantize_dual_validation(lib):
+    f = lib.jetfp8_quantize_act_dual
+    assert f(A16, 100, 128, B16, C16, D16, E16, None) == J.ERR_SHAPE      # M % 128
+    assert f(A16, 128, 100, B16, C16, D16, E16, None) == J.ERR_SHAPE      # K % 128
+    assert f(None, 0, 128, None, None, None, None, None) == J.OK
+    assert f(A16, 128, 128, B16, C16, None, E16, None) == J.ERR_INVALID_VALUE
+    assert f(A16, 128, 128, B16, C16, D16 + 4, E16, None) == J.ERR_ALIGNMENT
+    assert f(A16, 128, 128, B16, C16, B16 + 64, E16, None) == J.ERR_INVALID_VALUE   # qt overlaps q
+
+
 def test_quantize_weight_validation(lib):
     f = lib.jetfp8_quantize_weight
     assert f(A16, 100, 128, B16, C16, None, None) == J.ERR_SHAPE

@@ -159,6 +159,57 @@ def test_all_bf16_values_scale_one():
     assert_bitexact(q, oq, "codes")
 
 
+@pytest.mark.parametrize("M,K", [(128, 128), (256, 512), (384, 1152), (1024, 384), (128, 4096)])
+def test_dual_output_bitexact(M, K):
+    """One pass, both layouts: identical to the oracle's 1x128 and 128x1
+    quantisations and to the two single-output kernels."""
+    x = syn.activation(M, K, seed=M * 3 + K, outlier_scale=20.0)
+    xd = x.to(DEV)
+    q, s, qt, st = jf.quantize_act_dual(xd)
+    oq, os_ = oracle.quantize_act(bits(x))
+    oqt, ost = oracle.quantize_act_transposed(bits(x))
+    assert_bitexact(q, oq, "codes")
+    assert_bitexact(s, os_, "scales")
+    assert_bitexact(qt, oqt, "transposed codes")
+    assert_bitexact(st, ost, "transposed scales")
+    q1, s1 = jf.quantize_act(xd)
+    q2, s2 = jf.quantize_act_transposed(xd)
+    assert torch.equal(q, q1) and torch.equal(s, s1) and torch.equal(qt, q2) and torch.equal(st, s2)
+
+
+def test_dual_output_special_values():
+    x = torch.cat([special_values(128, 256, 4), tie_groups(128, 5).repeat(1, 2)], dim=0).contiguous()
+    q, s, qt, st = jf.quantize_act_dual(x.to(DEV))
+    oq, os_ = oracle.quantize_act(bits(x))
+    oqt, ost = oracle.quantize_act_transposed(bits(x))
+    assert_bitexact(q, oq, "codes")
+    assert_bitexact(s, os_, "scales")
+    assert_bitexact(qt, oqt, "transposed codes")
+    assert_bitexact(st, ost, "transposed scales")
+
+
+def test_dual_output_full_size_gradient():
+    """dY of the 8B gate_up projection [16384, 28672] through the dual kernel,
+    checked against the single-output kernels (themselves checked against the
+    oracle at this size above) and against the oracle on slices."""
+    M, N = 16384, 28672
+    dy = syn.grad_output(M, N, seed=6, device=DEV)
+    q, s, qt, st = jf.quantize_act_dual(dy)
+    q1, s1 = jf.quantize_act(dy)
+    assert torch.equal(q, q1) and torch.equal(s, s1)
+    del q1, s1
+    q2, s2 = jf.quantize_act_transposed(dy)
+    assert torch.equal(qt, q2) and torch.equal(st, s2)
+    del q2, s2
+    rows = slice(4096, 4096 + 256)
+    oq, os_ = oracle.quantize_act(bits(dy[rows]), threads=ORACLE_THREADS)
+    assert_bitexact(q[rows], oq, "codes (row block)")
+    sl = slice(N - 256, N)
+    oqt, ost = oracle.quantize_act_transposed(bits(dy[:, sl]), threads=ORACLE_THREADS)
+    assert_bitexact(qt[sl], oqt, "transposed codes (column block)")
+    assert_bitexact(st[:, sl].contiguous(), ost, "transposed scales (column block)")
+
+
 def test_empty_inputs():
     x = torch.empty(0, 256, dtype=torch.bfloat16, device=DEV)
     q, s = jf.quantize_act(x)

@@ -70,47 +70,52 @@ __device__ __forceinline__ GroupScale group_scale(float amax)
     return g;
 }
 
-// Codes of two values (lo's code in bits 0..7, hi's in bits 8..15) from the
-// lower bracket end; `mism` collects any disagreement with the upper end.
-__device__ __forceinline__ uint32_t encode2_fast(float lo, float hi, const GroupScale &g, uint32_t &mism)
-{
-    const uint32_t a = ptx::cvt_e4m3x2(lo * g.ra, hi * g.ra);
-    const uint32_t b = ptx::cvt_e4m3x2(lo * g.rb, hi * g.rb);
-    mism |= a ^ b;
-    return a;
-}
-
-// The same codes through the correctly rounded quotient.
-__device__ __forceinline__ uint32_t encode2_exact(float lo, float hi, float s)
-{
-    return ptx::cvt_e4m3x2(lo / s, hi / s);
-}
-
-// Codes of N consecutive values (N % 4 == 0) into N/4 little-endian words:
-// the bracket test first, the exact quotient for the whole run only if any
-// pair's bracket ends disagree (or the scale is subnormal).  A zero scale
-// (all-zero group) gives zero codes.
+// Codes of 4N consecutive values into N little-endian words (value i in
+// byte i of its word), from the lower bracket end, two values per packed
+// multiply.  Returns a mask with bit k set when word k needs the exact
+// quotient (some value's bracket ends disagree, or the scale is subnormal);
+// the caller recomputes those words with encode4_exact from a re-read of the
+// input.  A zero scale (all-zero group) gives zero codes and no work.
+// On normal-distributed bf16 data about 0.5 % of the values sit on or next to
+// a rounding midpoint (x / amax is a short binary fraction), so patching only
+// the flagged words keeps the exact path off the common path.
 template <int N>
-__device__ __forceinline__ void encode_run(const float *f, const GroupScale &g, uint32_t *w)
+__device__ __forceinline__ uint32_t encode_words(const float *f, const GroupScale &g, uint32_t *w)
 {
-    if (g.s == 0.0f) {
+    static_assert(N <= 32, "one mask bit per word");
+    if (g.s == 0.0f || !g.fast) {
 #pragma unroll
-        for (int i = 0; i < N / 4; ++i)
-            w[i] = 0u;
-        return;
+        for (int k = 0; k < N; ++k)
+            w[k] = 0u;
+        return g.s == 0.0f ? 0u : (N == 32 ? 0xffffffffu : ((1u << N) - 1u));
     }
-    uint32_t mism = g.fast ? 0u : 1u;
-    if (g.fast) {
+    const uint64_t ra2 = ptx::pack_f32x2(g.ra, g.ra), rb2 = ptx::pack_f32x2(g.rb, g.rb);
+    uint32_t mask = 0u;
 #pragma unroll
-        for (int i = 0; i < N / 4; ++i)
-            w[i] = encode2_fast(f[4 * i], f[4 * i + 1], g, mism) |
-                   (encode2_fast(f[4 * i + 2], f[4 * i + 3], g, mism) << 16);
+    for (int k = 0; k < N; ++k) {
+        const uint64_t x0 = ptx::pack_f32x2(f[4 * k], f[4 * k + 1]);
+        const uint64_t x1 = ptx::pack_f32x2(f[4 * k + 2], f[4 * k + 3]);
+        const uint64_t a0 = ptx::mul_f32x2(x0, ra2), b0 = ptx::mul_f32x2(x0, rb2);
+        const uint64_t a1 = ptx::mul_f32x2(x1, ra2), b1 = ptx::mul_f32x2(x1, rb2);
+        const uint32_t lo = ptx::cvt_e4m3x2(ptx::lo_f32(a0), ptx::hi_f32(a0)) |
+                            (ptx::cvt_e4m3x2(ptx::lo_f32(a1), ptx::hi_f32(a1)) << 16);
+        const uint32_t hi = ptx::cvt_e4m3x2(ptx::lo_f32(b0), ptx::hi_f32(b0)) |
+                            (ptx::cvt_e4m3x2(ptx::lo_f32(b1), ptx::hi_f32(b1)) << 16);
+        w[k] = lo;
+        mask |= (lo != hi ? 1u : 0u) << k;
     }
-    if (mism != 0u) {
-#pragma unroll
-        for (int i = 0; i < N / 4; ++i)
-            w[i] = encode2_exact(f[4 * i], f[4 * i + 1], g.s) | (encode2_exact(f[4 * i + 2], f[4 * i + 3], g.s) << 16);
-    }
+    return mask;
+}
+
+// Codes of four values through the correctly rounded quotient x / s.
+__device__ __forceinline__ uint32_t encode4_exact(float a, float b, float c, float d, float s)
+{
+    return ptx::cvt_e4m3x2(a / s, b / s) | (ptx::cvt_e4m3x2(c / s, d / s) << 16);
+}
+
+__device__ __forceinline__ uint32_t encode4_exact(uint2 bf16x4, float s)
+{
+    return encode4_exact(bf16_lo(bf16x4.x), bf16_hi(bf16x4.x), bf16_lo(bf16x4.y), bf16_hi(bf16x4.y), s);
 }
 
 // ---------------------------------------------------------------------------
@@ -168,13 +173,21 @@ quantize_act_kernel(const uint4 *__restrict__ x, int64_t M, int64_t K, uint2 *__
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
         const GroupScale gs = group_scale(amax);
         uint32_t w[8];
-        encode_run<32>(f, gs, w);
+        uint32_t redo = encode_words<8>(f, gs, w);
         if (m < M) {
 #pragma unroll
             for (int j = 0; j < 4; ++j)
                 __stcs(q + m * K8 + g * 16 + 4 * j + sub, make_uint2(w[2 * j], w[2 * j + 1]));
             if (sub == 0)
                 s[g * M + m] = gs.s;
+            // rare: words whose bracket disagreed get the exact quotient
+            while (redo != 0u) {
+                const int k = __ffs(redo) - 1;
+                redo &= redo - 1u;
+                const int64_t e = m * K + g * 128 + (4 * (k >> 1) + sub) * 8 + 4 * (k & 1);
+                const uint2 in = *reinterpret_cast<const uint2 *>(reinterpret_cast<const uint16_t *>(x) + e);
+                *reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(q) + e) = encode4_exact(in, gs.s);
+            }
         }
     }
 }
@@ -236,8 +249,7 @@ quantize_act_t_kernel(const uint4 *__restrict__ x, int64_t M, int64_t C, uint8_t
     }
     const GroupScale g0 = group_scale(a0), g1 = group_scale(a1);
     uint32_t w0[8], w1[8];
-    encode_run<32>(f0, g0, w0);
-    encode_run<32>(f1, g1, w1);
+    uint32_t redo = encode_words<8>(f0, g0, w0) | (encode_words<8>(f1, g1, w1) << 8);
     const int64_t col = c0 + 2 * lane;
     uint4 *d0 = reinterpret_cast<uint4 *>(qt + col * M + m0 + 32 * q);
     uint4 *d1 = reinterpret_cast<uint4 *>(qt + (col + 1) * M + m0 + 32 * q);
@@ -247,6 +259,21 @@ quantize_act_t_kernel(const uint4 *__restrict__ x, int64_t M, int64_t C, uint8_t
     __stcs(d1 + 1, make_uint4(w1[4], w1[5], w1[6], w1[7]));
     if (q == 0)
         *reinterpret_cast<float2 *>(st + (m0 >> 7) * C + col) = make_float2(g0.s, g1.s);
+    // rare: words whose bracket disagreed get the exact quotient (inputs re-read
+    // from the shared-memory tile: 4 rows of this thread's column)
+    while (redo != 0u) {
+        const int b = __ffs(redo) - 1;
+        redo &= redo - 1u;
+        const int hi = b >> 3, k = b & 7;
+        float v4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const uint32_t wv = reinterpret_cast<const uint32_t *>(&tile[32 * q + 4 * k + e][0])[lane];
+            v4[e] = hi ? bf16_hi(wv) : bf16_lo(wv);
+        }
+        *reinterpret_cast<uint32_t *>(qt + (col + hi) * M + m0 + 32 * q + 4 * k) =
+            encode4_exact(v4[0], v4[1], v4[2], v4[3], hi ? g1.s : g0.s);
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -294,17 +321,30 @@ quantize_weight_kernel(const uint4 *__restrict__ w, int64_t N, int64_t K, uint2 
     if (t == 0)
         s[bn * (K >> 7) + bk] = gs.s;
 
+    uint32_t redo = 0u;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         float f[8];
         unpack8(v[i], f);
-        uint32_t w[2];
-        encode_run<8>(f, gs, w);
-        const uint2 codes = make_uint2(w[0], w[1]);
+        uint32_t wd[2];
+        redo |= encode_words<2>(f, gs, wd) << (2 * i);
+        const uint2 codes = make_uint2(wd[0], wd[1]);
         const int r = r0 + 16 * i;
         __stcs(q + (bn * 128 + r) * K8 + bk * 16 + sub, codes);
         if (qt != nullptr)
             *reinterpret_cast<uint2 *>(&s_codes[r][sub * 8]) = codes;
+    }
+    // rare: words whose bracket disagreed get the exact quotient
+    while (redo != 0u) {
+        const int b = __ffs(redo) - 1;
+        redo &= redo - 1u;
+        const int r = r0 + 16 * (b >> 1), c = sub * 8 + 4 * (b & 1);
+        const int64_t e = (bn * 128 + r) * K + bk * 128 + c;
+        const uint32_t code =
+            encode4_exact(*reinterpret_cast<const uint2 *>(reinterpret_cast<const uint16_t *>(w) + e), gs.s);
+        *reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(q) + e) = code;
+        if (qt != nullptr)
+            *reinterpret_cast<uint32_t *>(&s_codes[r][c]) = code;
     }
     if (qt == nullptr)
         return;
@@ -388,13 +428,21 @@ quantize_act_dual_kernel(const uint4 *__restrict__ x, int64_t M, int64_t K, uint
         amax = fmaxf(s_ramax[0][r], s_ramax[1][r]);
         const GroupScale gs = group_scale(amax);
         uint32_t w[16];
-        encode_run<64>(f, gs, w);
-        uint4 *dst = reinterpret_cast<uint4 *>(q + (m0 + r) * K + k0 + 64 * h);
+        uint32_t redo = encode_words<16>(f, gs, w);
+        uint8_t *row_out = q + (m0 + r) * K + k0 + 64 * h;
+        uint4 *dst = reinterpret_cast<uint4 *>(row_out);
 #pragma unroll
         for (int j = 0; j < 4; ++j)
             __stcs(dst + j, make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]));
         if (h == 0)
             s[(k0 >> 7) * M + m0 + r] = gs.s;
+        // rare: words whose bracket disagreed get the exact quotient
+        while (redo != 0u) {
+            const int k = __ffs(redo) - 1;
+            redo &= redo - 1u;
+            const uint2 in = reinterpret_cast<const uint2 *>(&tile[r][(8 * h + (k >> 1)) ^ (r & 15)])[k & 1];
+            *reinterpret_cast<uint32_t *>(row_out + 4 * k) = encode4_exact(in, gs.s);
+        }
     }
 
     // ---- 128x1 groups along columns, written transposed -------------------
@@ -423,8 +471,7 @@ quantize_act_dual_kernel(const uint4 *__restrict__ x, int64_t M, int64_t K, uint
         }
         const GroupScale g0 = group_scale(a0), g1 = group_scale(a1);
         uint32_t w0[8], w1[8];
-        encode_run<32>(f0, g0, w0);
-        encode_run<32>(f1, g1, w1);
+        uint32_t redo = encode_words<8>(f0, g0, w0) | (encode_words<8>(f1, g1, w1) << 8);
         const int64_t col = k0 + 2 * p;
         uint4 *d0 = reinterpret_cast<uint4 *>(qt + col * M + m0 + 32 * qd);
         uint4 *d1 = reinterpret_cast<uint4 *>(qt + (col + 1) * M + m0 + 32 * qd);
@@ -434,6 +481,22 @@ quantize_act_dual_kernel(const uint4 *__restrict__ x, int64_t M, int64_t K, uint
         __stcs(d1 + 1, make_uint4(w1[4], w1[5], w1[6], w1[7]));
         if (qd == 0)
             *reinterpret_cast<float2 *>(st + (m0 >> 7) * K + col) = make_float2(g0.s, g1.s);
+        // rare: words whose bracket disagreed get the exact quotient
+        while (redo != 0u) {
+            const int b = __ffs(redo) - 1;
+            redo &= redo - 1u;
+            const int hi = b >> 3, k = b & 7;
+            float v4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int rr = 32 * qd + 4 * k + e;
+                const uint32_t wv =
+                    reinterpret_cast<const uint32_t *>(&tile[rr][0])[(((p >> 2) ^ (rr & 15)) << 2) + (p & 3)];
+                v4[e] = hi ? bf16_hi(wv) : bf16_lo(wv);
+            }
+            *reinterpret_cast<uint32_t *>(qt + (col + hi) * M + m0 + 32 * qd + 4 * k) =
+                encode4_exact(v4[0], v4[1], v4[2], v4[3], hi ? g1.s : g0.s);
+        }
     }
 }
 

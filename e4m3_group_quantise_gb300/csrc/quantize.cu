@@ -368,8 +368,9 @@ quantize_weight_kernel(const uint4 *__restrict__ w, int64_t N, int64_t K, uint2 
 // ---------------------------------------------------------------------------
 // Dual output: one read of X [M][K] yields both the 1x128 row-group codes and
 // scales (as quantize_act_kernel) and the 128x1 column-group codes and scales
-// written transposed (as quantize_act_t_kernel).  CTA tile: 128 rows x 128
-// columns of bf16 in shared memory, 16-byte chunks XOR-swizzled by
+// written transposed (as quantize_act_t_kernel).  Persistent CTAs walk 128 x
+// 128 tiles; each tile is copied (cp.async) into one of two shared-memory
+// buffers while the previous tile is quantised, 16-byte chunks XOR-swizzled by
 // (row & 15) so that both read patterns below are bank-conflict free.
 //   rows:    thread (r = t % 128, half h = t / 128) reads 64 values of row r;
 //            the two halves combine their amax through shared memory; each
@@ -381,123 +382,143 @@ quantize_weight_kernel(const uint4 *__restrict__ w, int64_t N, int64_t K, uint2 
 // ---------------------------------------------------------------------------
 constexpr int QD_TILE = 128;
 constexpr int QD_THREADS = 256;
+constexpr int QD_CTAS_PER_SM = 3;
 
-__global__ void __launch_bounds__(QD_THREADS)
-quantize_act_dual_kernel(const uint4 *__restrict__ x, int64_t M, int64_t K, uint8_t *__restrict__ q,
-                         float *__restrict__ s, uint8_t *__restrict__ qt, float *__restrict__ st)
+struct DualSmem {
+    uint4 tile[2][QD_TILE][QD_TILE / 8];
+    float ramax[2][QD_TILE];
+    float2 camax[4][QD_TILE / 2];
+};
+
+__device__ __forceinline__ void dual_issue_tile(DualSmem &sm, int buf, const uint4 *x, int64_t K8, int64_t m0,
+                                                int64_t k0, int t)
 {
-    __shared__ uint4 tile[QD_TILE][QD_TILE / 8];
-    __shared__ float s_ramax[2][QD_TILE];
-    __shared__ float2 s_camax[4][QD_TILE / 2];
-    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-    const int64_t m0 = static_cast<int64_t>(blockIdx.x) * QD_TILE;
-    const int64_t k0 = static_cast<int64_t>(blockIdx.y) * QD_TILE;
-    const int64_t K8 = K >> 3;
-
-    uint4 v[8];
 #pragma unroll
     for (int p = 0; p < 8; ++p) {
         const int idx = p * QD_THREADS + t;          // 16 chunks per row
-        v[p] = __ldcs(x + (m0 + (idx >> 4)) * K8 + (k0 >> 3) + (idx & 15));
-    }
-#pragma unroll
-    for (int p = 0; p < 8; ++p) {
-        const int idx = p * QD_THREADS + t;
         const int r = idx >> 4, c = idx & 15;
-        tile[r][c ^ (r & 15)] = v[p];
+        ptx::cp_async_16(&sm.tile[buf][r][c ^ (r & 15)], x + (m0 + r) * K8 + (k0 >> 3) + c);
     }
-    __syncthreads();
+}
 
-    // ---- 1x128 groups along rows -----------------------------------------
-    {
-        const int r = t & 127, h = t >> 7;
-        float f[64];
-        float amax = 0.0f;
+__global__ void __launch_bounds__(QD_THREADS, QD_CTAS_PER_SM)
+quantize_act_dual_kernel(const uint4 *__restrict__ x, int64_t M, int64_t K, uint8_t *__restrict__ q,
+                         float *__restrict__ s, uint8_t *__restrict__ qt, float *__restrict__ st)
+{
+    extern __shared__ __align__(16) uint8_t dual_smem_raw[];
+    DualSmem &sm = *reinterpret_cast<DualSmem *>(dual_smem_raw);
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const int64_t K8 = K >> 3;
+    const int64_t tiles_k = K / QD_TILE;
+    const int64_t n_tiles = (M / QD_TILE) * tiles_k;
+
+    int64_t tile = blockIdx.x;
+    if (tile < n_tiles)
+        dual_issue_tile(sm, 0, x, K8, (tile / tiles_k) * QD_TILE, (tile % tiles_k) * QD_TILE, t);
+    ptx::cp_async_commit();
+    for (int it = 0; tile < n_tiles; ++it, tile += gridDim.x) {
+        const int buf = it & 1;
+        const int64_t m0 = (tile / tiles_k) * QD_TILE, k0 = (tile % tiles_k) * QD_TILE;
+        const int64_t next = tile + gridDim.x;
+        if (next < n_tiles)
+            dual_issue_tile(sm, buf ^ 1, x, K8, (next / tiles_k) * QD_TILE, (next % tiles_k) * QD_TILE, t);
+        ptx::cp_async_commit();
+        ptx::cp_async_wait<1>();                      // this tile's copies have landed
+        __syncthreads();
+        const uint4 (*tl)[QD_TILE / 8] = sm.tile[buf];
+
+        // ---- 1x128 groups along rows -------------------------------------
+        {
+            const int r = t & 127, h = t >> 7;
+            float f[64];
+            float amax = 0.0f;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            float u[8];
-            unpack8(tile[r][(8 * h + j) ^ (r & 15)], u);
+            for (int j = 0; j < 8; ++j) {
+                float u[8];
+                unpack8(tl[r][(8 * h + j) ^ (r & 15)], u);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                f[8 * j + e] = u[e];
-                amax = fmaxf(amax, fabsf(u[e]));
+                for (int e = 0; e < 8; ++e) {
+                    f[8 * j + e] = u[e];
+                    amax = fmaxf(amax, fabsf(u[e]));
+                }
+            }
+            sm.ramax[h][r] = amax;
+            __syncthreads();
+            amax = fmaxf(sm.ramax[0][r], sm.ramax[1][r]);
+            const GroupScale gs = group_scale(amax);
+            uint32_t w[16];
+            uint32_t redo = encode_words<16>(f, gs, w);
+            uint8_t *row_out = q + (m0 + r) * K + k0 + 64 * h;
+            uint4 *dst = reinterpret_cast<uint4 *>(row_out);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                __stcs(dst + j, make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]));
+            if (h == 0)
+                s[(k0 >> 7) * M + m0 + r] = gs.s;
+            // rare: words whose bracket disagreed get the exact quotient
+            while (redo != 0u) {
+                const int k = __ffs(redo) - 1;
+                redo &= redo - 1u;
+                const uint2 in = reinterpret_cast<const uint2 *>(&tl[r][(8 * h + (k >> 1)) ^ (r & 15)])[k & 1];
+                *reinterpret_cast<uint32_t *>(row_out + 4 * k) = encode4_exact(in, gs.s);
             }
         }
-        s_ramax[h][r] = amax;
-        __syncthreads();
-        amax = fmaxf(s_ramax[0][r], s_ramax[1][r]);
-        const GroupScale gs = group_scale(amax);
-        uint32_t w[16];
-        uint32_t redo = encode_words<16>(f, gs, w);
-        uint8_t *row_out = q + (m0 + r) * K + k0 + 64 * h;
-        uint4 *dst = reinterpret_cast<uint4 *>(row_out);
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            __stcs(dst + j, make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]));
-        if (h == 0)
-            s[(k0 >> 7) * M + m0 + r] = gs.s;
-        // rare: words whose bracket disagreed get the exact quotient
-        while (redo != 0u) {
-            const int k = __ffs(redo) - 1;
-            redo &= redo - 1u;
-            const uint2 in = reinterpret_cast<const uint2 *>(&tile[r][(8 * h + (k >> 1)) ^ (r & 15)])[k & 1];
-            *reinterpret_cast<uint32_t *>(row_out + 4 * k) = encode4_exact(in, gs.s);
-        }
-    }
 
-    // ---- 128x1 groups along columns, written transposed -------------------
-    {
-        const int qd = warp >> 1;                   // row quarter
-        const int p = 32 * (warp & 1) + lane;       // column pair
-        float f0[32], f1[32];
-        float a0 = 0.0f, a1 = 0.0f;
+        // ---- 128x1 groups along columns, written transposed ---------------
+        {
+            const int qd = warp >> 1;                   // row quarter
+            const int p = 32 * (warp & 1) + lane;       // column pair
+            float f0[32], f1[32];
+            float a0 = 0.0f, a1 = 0.0f;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const int r = 32 * qd + i;
-            const uint32_t *row = reinterpret_cast<const uint32_t *>(&tile[r][0]);
-            const uint32_t wv = row[(((p >> 2) ^ (r & 15)) << 2) + (p & 3)];
-            f0[i] = bf16_lo(wv);
-            f1[i] = bf16_hi(wv);
-            a0 = fmaxf(a0, fabsf(f0[i]));
-            a1 = fmaxf(a1, fabsf(f1[i]));
-        }
-        s_camax[qd][p] = make_float2(a0, a1);
-        __syncthreads();
-#pragma unroll
-        for (int kq = 0; kq < 4; ++kq) {
-            const float2 o = s_camax[kq][p];
-            a0 = fmaxf(a0, o.x);
-            a1 = fmaxf(a1, o.y);
-        }
-        const GroupScale g0 = group_scale(a0), g1 = group_scale(a1);
-        uint32_t w0[8], w1[8];
-        uint32_t redo = encode_words<8>(f0, g0, w0) | (encode_words<8>(f1, g1, w1) << 8);
-        const int64_t col = k0 + 2 * p;
-        uint4 *d0 = reinterpret_cast<uint4 *>(qt + col * M + m0 + 32 * qd);
-        uint4 *d1 = reinterpret_cast<uint4 *>(qt + (col + 1) * M + m0 + 32 * qd);
-        __stcs(d0, make_uint4(w0[0], w0[1], w0[2], w0[3]));
-        __stcs(d0 + 1, make_uint4(w0[4], w0[5], w0[6], w0[7]));
-        __stcs(d1, make_uint4(w1[0], w1[1], w1[2], w1[3]));
-        __stcs(d1 + 1, make_uint4(w1[4], w1[5], w1[6], w1[7]));
-        if (qd == 0)
-            *reinterpret_cast<float2 *>(st + (m0 >> 7) * K + col) = make_float2(g0.s, g1.s);
-        // rare: words whose bracket disagreed get the exact quotient
-        while (redo != 0u) {
-            const int b = __ffs(redo) - 1;
-            redo &= redo - 1u;
-            const int hi = b >> 3, k = b & 7;
-            float v4[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int rr = 32 * qd + 4 * k + e;
-                const uint32_t wv =
-                    reinterpret_cast<const uint32_t *>(&tile[rr][0])[(((p >> 2) ^ (rr & 15)) << 2) + (p & 3)];
-                v4[e] = hi ? bf16_hi(wv) : bf16_lo(wv);
+            for (int i = 0; i < 32; ++i) {
+                const int r = 32 * qd + i;
+                const uint32_t wv = reinterpret_cast<const uint32_t *>(&tl[r][0])[(((p >> 2) ^ (r & 15)) << 2) + (p & 3)];
+                f0[i] = bf16_lo(wv);
+                f1[i] = bf16_hi(wv);
+                a0 = fmaxf(a0, fabsf(f0[i]));
+                a1 = fmaxf(a1, fabsf(f1[i]));
             }
-            *reinterpret_cast<uint32_t *>(qt + (col + hi) * M + m0 + 32 * qd + 4 * k) =
-                encode4_exact(v4[0], v4[1], v4[2], v4[3], hi ? g1.s : g0.s);
+            sm.camax[qd][p] = make_float2(a0, a1);
+            __syncthreads();
+#pragma unroll
+            for (int kq = 0; kq < 4; ++kq) {
+                const float2 o = sm.camax[kq][p];
+                a0 = fmaxf(a0, o.x);
+                a1 = fmaxf(a1, o.y);
+            }
+            const GroupScale g0 = group_scale(a0), g1 = group_scale(a1);
+            uint32_t w0[8], w1[8];
+            uint32_t redo = encode_words<8>(f0, g0, w0) | (encode_words<8>(f1, g1, w1) << 8);
+            const int64_t col = k0 + 2 * p;
+            uint4 *d0 = reinterpret_cast<uint4 *>(qt + col * M + m0 + 32 * qd);
+            uint4 *d1 = reinterpret_cast<uint4 *>(qt + (col + 1) * M + m0 + 32 * qd);
+            __stcs(d0, make_uint4(w0[0], w0[1], w0[2], w0[3]));
+            __stcs(d0 + 1, make_uint4(w0[4], w0[5], w0[6], w0[7]));
+            __stcs(d1, make_uint4(w1[0], w1[1], w1[2], w1[3]));
+            __stcs(d1 + 1, make_uint4(w1[4], w1[5], w1[6], w1[7]));
+            if (qd == 0)
+                *reinterpret_cast<float2 *>(st + (m0 >> 7) * K + col) = make_float2(g0.s, g1.s);
+            // rare: words whose bracket disagreed get the exact quotient
+            while (redo != 0u) {
+                const int b2 = __ffs(redo) - 1;
+                redo &= redo - 1u;
+                const int hi = b2 >> 3, k = b2 & 7;
+                float v4[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int rr = 32 * qd + 4 * k + e;
+                    const uint32_t wv =
+                        reinterpret_cast<const uint32_t *>(&tl[rr][0])[(((p >> 2) ^ (rr & 15)) << 2) + (p & 3)];
+                    v4[e] = hi ? bf16_hi(wv) : bf16_lo(wv);
+                }
+                *reinterpret_cast<uint32_t *>(qt + (col + hi) * M + m0 + 32 * qd + 4 * k) =
+                    encode4_exact(v4[0], v4[1], v4[2], v4[3], hi ? g1.s : g0.s);
+            }
         }
+        __syncthreads();                                // buffer `buf` is refilled two tiles on
     }
+    ptx::cp_async_wait<0>();
 }
 
 }  // namespace
@@ -535,8 +556,18 @@ namespace jetfp8 {
 cudaError_t launch_quantize_act_dual(const void *x, int64_t M, int64_t K, uint8_t *q, float *s, uint8_t *qt,
                                      float *st, cudaStream_t stream)
 {
-    dim3 grid(static_cast<unsigned>(M / QD_TILE), static_cast<unsigned>(K / QD_TILE));
-    quantize_act_dual_kernel<<<grid, QD_THREADS, 0, stream>>>(static_cast<const uint4 *>(x), M, K, q, s, qt, st);
+    static_assert(sizeof(DualSmem) <= 227 * 1024 / QD_CTAS_PER_SM, "dual tile buffers exceed shared memory");
+    cudaError_t e = cudaFuncSetAttribute(quantize_act_dual_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(sizeof(DualSmem)));
+    if (e != cudaSuccess)
+        return e;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t tiles = (M / QD_TILE) * (K / QD_TILE);
+    const int64_t grid = tiles < int64_t(sms) * QD_CTAS_PER_SM ? tiles : int64_t(sms) * QD_CTAS_PER_SM;
+    quantize_act_dual_kernel<<<static_cast<unsigned>(grid), QD_THREADS, sizeof(DualSmem), stream>>>(
+        static_cast<const uint4 *>(x), M, K, q, s, qt, st);
     return cudaGetLastError();
 }
 }  // namespace jetfp8

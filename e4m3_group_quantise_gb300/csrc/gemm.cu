@@ -32,11 +32,11 @@
 //                                      stages 32 rows x 16 columns in shared
 //                                      memory and TMA-stores them (double-
 //                                      buffered, asynchronous)
-// Registers are rebalanced with setmaxnreg: the control warpgroup drops to 40
-// per thread and the promotion warpgroups rise to 232 (128*40 + 256*232 =
-// 64512 = 384 threads * 168, the launch allocation).
-// Tile BM = 128 rows x BN (256 or 128) columns; one pipeline stage per
-// 128-wide K group (the scale granularity).  Every wait is bounded: a
+// Registers are rebalanced with setmaxnreg: the control warpgroup drops to 88
+// per thread and the promotion warpgroups rise to 200 (128*88 + 256*200 =
+// 62464 <= 64512 = 384 threads * 168, the launch allocation).
+// Tile BM = 128 rows x BN = 128 columns; large problems run CTA pairs (see
+// PAIR below); one pipeline stage per 128-wide K group (the scale granularity).  Every wait is bounded: a
 // wait that runs out sets the device error word, the CTA drains its copies
 // and MMAs in flight, frees its tensor memory and exits.
 #include <cuda.h>
@@ -58,8 +58,8 @@ constexpr int MMA_WARP = 1;
 constexpr int SCALE_WARP = 2;
 constexpr int FIRST_PROMO_WARP = 4;
 constexpr int SCALE_STAGES = 4;
-constexpr uint32_t CTRL_REGS = 40;
-constexpr uint32_t PROMO_REGS = 232;
+constexpr uint32_t CTRL_REGS = 88;
+constexpr uint32_t PROMO_REGS = 200;
 static_assert(128 * CTRL_REGS + 256 * PROMO_REGS <= NUM_THREADS * 168, "register split exceeds the launch allocation");
 constexpr int GROUP_M = 16;              // tile rasterisation: m-tiles per band
 constexpr uint64_t WAIT_TIMEOUT_NS = 2000000000ull;   // 2 s
@@ -73,6 +73,7 @@ struct KernelArgs {
     uint32_t *err;
     int32_t rows, cols, groups;
     int32_t tiles_m, tiles_n;
+    int32_t tiles_nw;     // work-item columns: tiles_n, or tile pairs (ceil(tiles_n / 2)) for CTA pairs
 };
 
 template <int BN, int STAGES>
@@ -90,8 +91,8 @@ struct Smem {
     static constexpr uint32_t OUT_CHUNK_BYTES = 32 * 16 * 2;
     static constexpr uint32_t OUT_BYTES = 8 * 2 * OUT_CHUNK_BYTES;
     static constexpr uint32_t BAR_OFF = OUT_OFF + OUT_BYTES;
-    // full[S], empty[S], sfull[SS], sempty[SS], tfull[2], tempty[2], mma_done, tmem holder, abort flag
-    static constexpr uint32_t CTRL_BYTES = (2 * STAGES + 2 * SCALE_STAGES + 5) * 8 + 16;
+    // full[S], empty[S], sfull[SS], sempty[SS], tfull[4], tempty[4], mma_done, tmem holder, abort flag
+    static constexpr uint32_t CTRL_BYTES = (2 * STAGES + 2 * SCALE_STAGES + 9) * 8 + 16;
     static constexpr uint32_t TOTAL = 1024 /* alignment slack */ + BAR_OFF + CTRL_BYTES;
 };
 
@@ -112,7 +113,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
-template <int BN, int STAGES, bool SB_PER_COLUMN>
+// PAIR: the kernel runs as clusters of two CTAs that compute horizontally
+// adjacent 128 x BN tiles (same rows).  Each CTA loads half of the shared A
+// tile and multicasts it to both; a stage is refilled only after both CTAs'
+// MMAs have released it (each MMA issuer's commit arrives on both CTAs' empty
+// barriers).  With BN = 128 this halves each SM's accumulator tile, so TMEM
+// holds four partial buffers (the release chain then overlaps three groups of
+// MMAs) while the L2 traffic per FLOP stays that of a 128 x 256 tile.
+template <int BN, int STAGES, bool SB_PER_COLUMN, bool PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
             const __grid_constant__ CUtensorMap tmap_d, const KernelArgs args)
@@ -121,7 +129,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     constexpr int COLS_PER_WG = BN / 2;          // columns per promotion warpgroup
     constexpr int CHUNKS = COLS_PER_WG / 32;     // tcgen05.ld x32 per group
     static_assert(CHUNKS % 2 == 0, "loads are issued in pairs");
-    constexpr uint32_t TMEM_COLS = 2 * BN;       // two partial buffers
+    constexpr uint32_t NBUF = PAIR ? 4 : 2;      // TMEM partial buffers
+    constexpr uint32_t TMEM_COLS = NBUF * BN;
+    static_assert(TMEM_COLS <= 512, "TMEM holds 512 columns");
     constexpr uint32_t IDESC = ptx::idesc_e4m3_f32(BM, BN);
 
     extern __shared__ uint8_t smem_raw[];
@@ -134,27 +144,36 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     uint64_t *sfull = empty + STAGES;
     uint64_t *sempty = sfull + SCALE_STAGES;
     uint64_t *tfull = sempty + SCALE_STAGES;
-    uint64_t *tempty = tfull + 2;
-    uint64_t *mma_done = tempty + 2;
+    uint64_t *tempty = tfull + 4;
+    uint64_t *mma_done = tempty + 4;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(mma_done + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int num_tiles = args.tiles_m * args.tiles_n;
     const int G = args.groups;
+    // work items: tiles, or (for CTA pairs) tile pairs shared by the cluster
+    const int num_work = args.tiles_m * args.tiles_nw;
+    const int work_first = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+    const int work_stride = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+    const int rank = PAIR ? static_cast<int>(ptx::cluster_ctarank()) : 0;
+    auto coords = [&](int w, int &tm, int &tn) {
+        tile_coords(w, args.tiles_m, args.tiles_nw, tm, tn);
+        if (PAIR)
+            tn = 2 * tn + rank;
+    };
 
     if (warp == PRODUCER_WARP) {
         if (lane == 0) {
             for (int s = 0; s < STAGES; ++s) {
                 ptx::mbar_init(&full[s], 1);
-                ptx::mbar_init(&empty[s], 1);
+                ptx::mbar_init(&empty[s], PAIR ? 2 : 1);   // both CTAs' MMA issuers for pairs
             }
             for (int s = 0; s < SCALE_STAGES; ++s) {
                 ptx::mbar_init(&sfull[s], 32);   // every loader lane's copies
                 ptx::mbar_init(&sempty[s], 8);   // one arrival per promotion warp
             }
-            for (int b = 0; b < 2; ++b) {
+            for (uint32_t b = 0; b < NBUF; ++b) {
                 ptx::mbar_init(&tfull[b], 1);
                 ptx::mbar_init(&tempty[b], 8);   // one arrival per promotion warp
             }
@@ -171,6 +190,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
+    if (PAIR)
+        ptx::cluster_sync();   // the peer's barriers exist before any multicast reaches them
     const uint32_t tmem_base = *tmem_holder;
 
     if (warp < FIRST_PROMO_WARP) {
@@ -182,9 +203,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                 uint32_t phase = 0;
                 uint32_t issued_mask = 0, issued_parity = 0;
                 bool ok = true;
-                for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+                for (int tile = work_first; ok && tile < num_work; tile += work_stride) {
                     int tm, tn;
-                    tile_coords(tile, args.tiles_m, args.tiles_n, tm, tn);
+                    coords(tile, tm, tn);
                     for (int g = 0; g < G; ++g) {
                         if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, args.err, ERRBIT_PRODUCER,
                                             WAIT_TIMEOUT_NS)) {
@@ -192,7 +213,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                             break;
                         }
                         ptx::mbar_arrive_expect_tx(&full[stage], L::STAGE_BYTES);
-                        ptx::tma_load_2d(sA + stage * L::A_BYTES, &tmap_a, &full[stage], g * BK, tm * BM);
+                        if (PAIR)   // this CTA's half of the shared A tile, to both CTAs
+                            ptx::tma_load_2d_multicast(sA + stage * L::A_BYTES + rank * (L::A_BYTES / 2), &tmap_a,
+                                                       &full[stage], g * BK, tm * BM + rank * (BM / 2), 0x3);
+                        else
+                            ptx::tma_load_2d(sA + stage * L::A_BYTES, &tmap_a, &full[stage], g * BK, tm * BM);
                         ptx::tma_load_2d(sB + stage * L::B_BYTES, &tmap_b, &full[stage], g * BK, tn * BN);
                         issued_mask |= 1u << stage;
                         issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -220,10 +245,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                 bool ok = true;
                 const uint32_t a_base = ptx::smem_u32(sA);
                 const uint32_t b_base = ptx::smem_u32(sB);
-                for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+                for (int tile = work_first; ok && tile < num_work; tile += work_stride) {
                     for (int g = 0; g < G; ++g, ++it) {
-                        const uint32_t buf = it & 1u;
-                        const uint32_t bphase = (it >> 1) & 1u;
+                        const uint32_t buf = it % NBUF;
+                        const uint32_t bphase = (it / NBUF) & 1u;
                         if (!ptx::mbar_wait(&tempty[buf], bphase ^ 1u, abort_flag, args.err, ERRBIT_MMA_TMEM,
                                             WAIT_TIMEOUT_NS) ||
                             !ptx::mbar_wait(&full[stage], phase, abort_flag, args.err, ERRBIT_MMA_SMEM,
@@ -238,7 +263,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
 #pragma unroll
                         for (int j = 0; j < BK / 32; ++j)   // 32 bytes of K per instruction: +2 in the >>4 field
                             ptx::mma_f8(d_tmem, adesc + 2 * j, bdesc + 2 * j, IDESC, j > 0 ? 1u : 0u);
-                        ptx::mma_commit(&empty[stage]);
+                        if (PAIR)
+                            ptx::mma_commit_multicast(&empty[stage], 0x3);
+                        else
+                            ptx::mma_commit(&empty[stage]);
                         ptx::mma_commit(&tfull[buf]);
                         if (++stage == STAGES) {
                             stage = 0;
@@ -256,9 +284,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
             int ss = 0;
             uint32_t sphase = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+            for (int tile = work_first; ok && tile < num_work; tile += work_stride) {
                 int tm, tn;
-                tile_coords(tile, args.tiles_m, args.tiles_n, tm, tn);
+                coords(tile, tm, tn);
                 for (int g = 0; g < G; ++g) {
                     if (!ptx::mbar_wait(&sempty[ss], sphase ^ 1u, abort_flag, args.err, ERRBIT_PROMOTE,
                                         WAIT_TIMEOUT_NS)) {
@@ -310,9 +338,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         int ss = 0;
         uint32_t sphase = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        for (int tile = work_first; ok && tile < num_work; tile += work_stride) {
             int tm, tn;
-            tile_coords(tile, args.tiles_m, args.tiles_n, tm, tn);
+            coords(tile, tm, tn);
             const int col0 = tn * BN + wg * COLS_PER_WG;
             uint64_t acc[COLS_PER_WG / 2];               // fp32 pairs: columns 2i, 2i+1
 #pragma unroll
@@ -320,8 +348,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                 acc[i] = 0ull;
 
             for (int g = 0; g < G; ++g, ++it) {
-                const uint32_t buf = it & 1u;
-                const uint32_t bphase = (it >> 1) & 1u;
+                const uint32_t buf = it % NBUF;
+                const uint32_t bphase = (it / NBUF) & 1u;
                 if (!ptx::mbar_wait(&sfull[ss], sphase, abort_flag, args.err, ERRBIT_PROMOTE, WAIT_TIMEOUT_NS)) {
                     ok = false;
                     break;
@@ -437,14 +465,16 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     ptx::tc_fence_after();
     if (warp == PRODUCER_WARP)
         ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+    if (PAIR)
+        ptx::cluster_sync();   // neither CTA leaves while the other may still write to it
 }
 
-template <int BN, int STAGES, bool SB_PER_COLUMN>
+template <int BN, int STAGES, bool SB_PER_COLUMN, bool PAIR>
 cudaError_t launch_variant(const GemmProblem &p, const DeviceInfo &dev, const CUtensorMap &ta, const CUtensorMap &tb,
                            const CUtensorMap &td, cudaStream_t stream)
 {
     using L = Smem<BN, STAGES>;
-    auto kern = gemm_kernel<BN, STAGES, SB_PER_COLUMN>;
+    auto kern = gemm_kernel<BN, STAGES, SB_PER_COLUMN, PAIR>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(L::TOTAL));
     if (e != cudaSuccess)
         return e;
@@ -460,9 +490,36 @@ cudaError_t launch_variant(const GemmProblem &p, const DeviceInfo &dev, const CU
     a.groups = static_cast<int32_t>(p.kdim / BK);
     a.tiles_m = static_cast<int32_t>((p.rows + BM - 1) / BM);
     a.tiles_n = static_cast<int32_t>((p.cols + BN - 1) / BN);
-    const int tiles = a.tiles_m * a.tiles_n;
-    const int grid = tiles < dev.sm_count ? tiles : dev.sm_count;
-    kern<<<grid, NUM_THREADS, L::TOTAL, stream>>>(ta, tb, td, a);
+    a.tiles_nw = PAIR ? (a.tiles_n + 1) / 2 : a.tiles_n;
+    const int work = a.tiles_m * a.tiles_nw;
+    if (!PAIR) {
+        const int grid = work < dev.sm_count ? work : dev.sm_count;
+        kern<<<grid, NUM_THREADS, L::TOTAL, stream>>>(ta, tb, td, a);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = L::TOTAL;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * work));
+    int clusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+    if (e != cudaSuccess)
+        return e;
+    if (clusters < 1)
+        return cudaErrorLaunchOutOfResources;
+    const int n = work < clusters ? work : clusters;
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * n));
+    e = cudaLaunchKernelEx(&cfg, kern, ta, tb, td, a);
+    if (e != cudaSuccess)
+        return e;
     return cudaGetLastError();
 }
 
@@ -496,21 +553,21 @@ CUresult encode_output(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap *ma
 cudaError_t launch_gemm(const GemmProblem &p, const DeviceInfo &dev, PFN_cuTensorMapEncodeTiled_v12000 encode,
                         cudaStream_t stream)
 {
-    // Wide tiles unless they would leave most SMs idle (small problems).
+    // Large problems: CTA pairs of 128 x 128 tiles sharing A (multicast).
+    // Small ones (fewer 128 x 256 tiles than SMs): single CTAs of 128 x 128.
     const int64_t tiles256 = ((p.rows + BM - 1) / BM) * ((p.cols + 255) / 256);
-    const bool wide = tiles256 >= dev.sm_count;
-    const int bn = wide ? 256 : 128;
+    const bool pair = tiles256 >= dev.sm_count;
     CUtensorMap ta, tb, td;
-    if (encode_operand(encode, &ta, p.a, p.rows, p.kdim, BM) != CUDA_SUCCESS ||
-        encode_operand(encode, &tb, p.b, p.cols, p.kdim, bn) != CUDA_SUCCESS ||
+    if (encode_operand(encode, &ta, p.a, p.rows, p.kdim, pair ? BM / 2 : BM) != CUDA_SUCCESS ||
+        encode_operand(encode, &tb, p.b, p.cols, p.kdim, 128) != CUDA_SUCCESS ||
         encode_output(encode, &td, p.d, p.rows, p.cols) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     const bool per_col = p.sb_mode == ScaleB::PerColumn;
-    if (wide)
-        return per_col ? launch_variant<256, 4, true>(p, dev, ta, tb, td, stream)
-                       : launch_variant<256, 4, false>(p, dev, ta, tb, td, stream);
-    return per_col ? launch_variant<128, 6, true>(p, dev, ta, tb, td, stream)
-                   : launch_variant<128, 6, false>(p, dev, ta, tb, td, stream);
+    if (pair)
+        return per_col ? launch_variant<128, 6, true, true>(p, dev, ta, tb, td, stream)
+                       : launch_variant<128, 6, false, true>(p, dev, ta, tb, td, stream);
+    return per_col ? launch_variant<128, 6, true, false>(p, dev, ta, tb, td, stream)
+                   : launch_variant<128, 6, false, false>(p, dev, ta, tb, td, stream);
 }
 
 // ---------------------------------------------------------------------------

@@ -117,6 +117,15 @@ def test_many_tiles_persistent_loop():
     run_wgrad(1024, 2048, 4096, 7, sample=2048)
 
 
+def test_pair_path_odd_tiles_and_ragged_rows():
+    """Problems large enough for the CTA-pair kernel, with an odd number of
+    128-column tiles (the second CTA of the last pair lies wholly outside the
+    output) and a ragged last row tile."""
+    run_fprop(19207, 384, 256, 41, sample=4096)
+    run_dgrad(19207, 256, 384, 42, sample=4096)
+    run_wgrad(256, 19200, 384, 43, sample=4096)
+
+
 # ------------------------------------------------------------ decode shapes
 @pytest.mark.parametrize("proj", list(syn.PROJ_8B))
 @pytest.mark.parametrize("M", [64, 256])

@@ -32,11 +32,11 @@
 //                                      stages 32 rows x 16 columns in shared
 //                                      memory and TMA-stores them (double-
 //                                      buffered, asynchronous)
-// Registers are rebalanced with setmaxnreg: the control warpgroup drops to 88
-// per thread and the promotion warpgroups rise to 200 (128*88 + 256*200 =
-// 62464 <= 64512 = 384 threads * 168, the launch allocation).
-// Tile BM = 128 rows x BN = 128 columns; large problems run CTA pairs (see
-// PAIR below); one pipeline stage per 128-wide K group (the scale granularity).  Every wait is bounded: a
+// Registers are rebalanced with setmaxnreg (RegSplit): with 128 x 256 tiles
+// the control warpgroup drops to 40 per thread and the promotion warpgroups
+// rise to 232 (128*40 + 256*232 = 64512 = 384 threads * 168, the launch
+// allocation).  Tile BM = 128 rows x BN (256, or 128 for small problems)
+// columns; one pipeline stage per 128-wide K group (the scale granularity).  Every wait is bounded: a
 // wait that runs out sets the device error word, the CTA drains its copies
 // and MMAs in flight, frees its tensor memory and exits.
 #include <cuda.h>
@@ -58,9 +58,13 @@ constexpr int MMA_WARP = 1;
 constexpr int SCALE_WARP = 2;
 constexpr int FIRST_PROMO_WARP = 4;
 constexpr int SCALE_STAGES = 4;
-constexpr uint32_t CTRL_REGS = 88;
-constexpr uint32_t PROMO_REGS = 200;
-static_assert(128 * CTRL_REGS + 256 * PROMO_REGS <= NUM_THREADS * 168, "register split exceeds the launch allocation");
+// setmaxnreg split per tile width: wide tiles keep 128 accumulator registers
+// per promotion thread, 128-wide tiles 64 (which leaves the control warps room).
+template <int BN> struct RegSplit;
+template <> struct RegSplit<256> { static constexpr uint32_t CTRL = 40, PROMO = 232; };
+template <> struct RegSplit<128> { static constexpr uint32_t CTRL = 88, PROMO = 200; };
+static_assert(128 * RegSplit<256>::CTRL + 256 * RegSplit<256>::PROMO <= NUM_THREADS * 168, "register split");
+static_assert(128 * RegSplit<128>::CTRL + 256 * RegSplit<128>::PROMO <= NUM_THREADS * 168, "register split");
 constexpr int GROUP_M = 16;              // tile rasterisation: m-tiles per band
 constexpr uint64_t WAIT_TIMEOUT_NS = 2000000000ull;   // 2 s
 
@@ -195,7 +199,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     const uint32_t tmem_base = *tmem_holder;
 
     if (warp < FIRST_PROMO_WARP) {
-        ptx::setmaxnreg_dec<CTRL_REGS>();
+        ptx::setmaxnreg_dec<RegSplit<BN>::CTRL>();
         if (warp == PRODUCER_WARP) {
             // -------------------------------------------------- TMA producer
             if (lane == 0) {
@@ -328,7 +332,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
             ptx::cp_async_wait_all();
         }
     } else {
-        ptx::setmaxnreg_inc<PROMO_REGS>();
+        ptx::setmaxnreg_inc<RegSplit<BN>::PROMO>();
         // ------------------------------------------------------ promotion
         const int wg = (warp - FIRST_PROMO_WARP) >> 2;   // 0 or 1: column half of the tile
         const int quarter = warp & 3;                    // TMEM lanes 32*quarter .. +31
@@ -553,19 +557,24 @@ CUresult encode_output(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap *ma
 cudaError_t launch_gemm(const GemmProblem &p, const DeviceInfo &dev, PFN_cuTensorMapEncodeTiled_v12000 encode,
                         cudaStream_t stream)
 {
-    // Large problems: CTA pairs of 128 x 128 tiles sharing A (multicast).
-    // Small ones (fewer 128 x 256 tiles than SMs): single CTAs of 128 x 128.
+    // 128 x 256 tiles, unless they would leave most SMs idle (small problems):
+    // then 128 x 128 tiles.
     const int64_t tiles256 = ((p.rows + BM - 1) / BM) * ((p.cols + 255) / 256);
-    const bool pair = tiles256 >= dev.sm_count;
+    const bool wide = tiles256 >= dev.sm_count;
+    const bool pair = false;   // CTA pairs of 128 x 128 tiles: measured slower than wide tiles so far
+    const int bn = (wide && !pair) ? 256 : 128;
     CUtensorMap ta, tb, td;
     if (encode_operand(encode, &ta, p.a, p.rows, p.kdim, pair ? BM / 2 : BM) != CUDA_SUCCESS ||
-        encode_operand(encode, &tb, p.b, p.cols, p.kdim, 128) != CUDA_SUCCESS ||
+        encode_operand(encode, &tb, p.b, p.cols, p.kdim, bn) != CUDA_SUCCESS ||
         encode_output(encode, &td, p.d, p.rows, p.cols) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     const bool per_col = p.sb_mode == ScaleB::PerColumn;
     if (pair)
         return per_col ? launch_variant<128, 6, true, true>(p, dev, ta, tb, td, stream)
                        : launch_variant<128, 6, false, true>(p, dev, ta, tb, td, stream);
+    if (wide)
+        return per_col ? launch_variant<256, 4, true, false>(p, dev, ta, tb, td, stream)
+                       : launch_variant<256, 4, false, false>(p, dev, ta, tb, td, stream);
     return per_col ? launch_variant<128, 6, true, false>(p, dev, ta, tb, td, stream)
                    : launch_variant<128, 6, false, false>(p, dev, ta, tb, td, stream);
 }

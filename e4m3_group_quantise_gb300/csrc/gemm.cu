@@ -346,10 +346,17 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
             int tm, tn;
             coords(tile, tm, tn);
             const int col0 = tn * BN + wg * COLS_PER_WG;
-            uint64_t acc[COLS_PER_WG / 2];               // fp32 pairs: columns 2i, 2i+1
+            // fp32 accumulators of this thread's row: packed pairs (columns 2i,
+            // 2i+1) with one scale per 128-column block, plain floats with a
+            // scale per column
+            uint64_t acc2[SB_PER_COLUMN ? 1 : COLS_PER_WG / 2];
+            float acc1[SB_PER_COLUMN ? COLS_PER_WG : 1];
 #pragma unroll
-            for (int i = 0; i < COLS_PER_WG / 2; ++i)
-                acc[i] = 0ull;
+            for (int i = 0; i < (SB_PER_COLUMN ? 1 : COLS_PER_WG / 2); ++i)
+                acc2[i] = 0ull;
+#pragma unroll
+            for (int i = 0; i < (SB_PER_COLUMN ? COLS_PER_WG : 1); ++i)
+                acc1[i] = 0.0f;
 
             for (int g = 0; g < G; ++g, ++it) {
                 const uint32_t buf = it % NBUF;
@@ -392,20 +399,27 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                         if (lane == 0)
                             ptx::mbar_arrive(&tempty[buf]);
                     }
-                    uint64_t *a0 = acc + h * 32;
                     if (SB_PER_COLUMN) {
-                        // acc += p * (sa * sb[col]), two columns per instruction
+                        // acc += p * (sa * sb[col]): the products two at a time,
+                        // the accumulation in plain fp32 FMAs
                         const uint64_t sa2 = ptx::pack_f32x2(sa, sa);
                         const uint64_t *sbv = reinterpret_cast<const uint64_t *>(sbcol + h * 64);
+                        float *a = acc1 + h * 64;
 #pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            ptx::fma_f32x2(a0[i], ptx::pack_f32x2(p0[2 * i], p0[2 * i + 1]), ptx::mul_f32x2(sa2, sbv[i]));
+                        for (int i = 0; i < 16; ++i) {
+                            const uint64_t w = ptx::mul_f32x2(sa2, sbv[i]);
+                            a[2 * i] = fmaf(__uint_as_float(p0[2 * i]), ptx::lo_f32(w), a[2 * i]);
+                            a[2 * i + 1] = fmaf(__uint_as_float(p0[2 * i + 1]), ptx::hi_f32(w), a[2 * i + 1]);
+                        }
 #pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            ptx::fma_f32x2(a0[16 + i], ptx::pack_f32x2(p1[2 * i], p1[2 * i + 1]),
-                                           ptx::mul_f32x2(sa2, sbv[16 + i]));
+                        for (int i = 0; i < 16; ++i) {
+                            const uint64_t w = ptx::mul_f32x2(sa2, sbv[16 + i]);
+                            a[32 + 2 * i] = fmaf(__uint_as_float(p1[2 * i]), ptx::lo_f32(w), a[32 + 2 * i]);
+                            a[32 + 2 * i + 1] = fmaf(__uint_as_float(p1[2 * i + 1]), ptx::hi_f32(w), a[32 + 2 * i + 1]);
+                        }
                     } else {
                         const uint64_t w2 = ptx::pack_f32x2(w_blk, w_blk);
+                        uint64_t *a0 = acc2 + h * 32;
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
                             ptx::fma_f32x2(a0[i], ptx::pack_f32x2(p0[2 * i], p0[2 * i + 1]), w2);
@@ -438,15 +452,19 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                     __syncwarp();
                     uint4 *dst = reinterpret_cast<uint4 *>(chunk + lane * 32);
                     uint4 o0, o1;
-                    const uint64_t *ac = acc + 8 * c;
-                    o0.x = pack_bf16x2(ptx::lo_f32(ac[0]), ptx::hi_f32(ac[0]));
-                    o0.y = pack_bf16x2(ptx::lo_f32(ac[1]), ptx::hi_f32(ac[1]));
-                    o0.z = pack_bf16x2(ptx::lo_f32(ac[2]), ptx::hi_f32(ac[2]));
-                    o0.w = pack_bf16x2(ptx::lo_f32(ac[3]), ptx::hi_f32(ac[3]));
-                    o1.x = pack_bf16x2(ptx::lo_f32(ac[4]), ptx::hi_f32(ac[4]));
-                    o1.y = pack_bf16x2(ptx::lo_f32(ac[5]), ptx::hi_f32(ac[5]));
-                    o1.z = pack_bf16x2(ptx::lo_f32(ac[6]), ptx::hi_f32(ac[6]));
-                    o1.w = pack_bf16x2(ptx::lo_f32(ac[7]), ptx::hi_f32(ac[7]));
+                    float v[16];
+#pragma unroll
+                    for (int k = 0; k < 16; ++k)
+                        v[k] = SB_PER_COLUMN ? acc1[16 * c + k]
+                                             : ((k & 1) ? ptx::hi_f32(acc2[8 * c + k / 2]) : ptx::lo_f32(acc2[8 * c + k / 2]));
+                    o0.x = pack_bf16x2(v[0], v[1]);
+                    o0.y = pack_bf16x2(v[2], v[3]);
+                    o0.z = pack_bf16x2(v[4], v[5]);
+                    o0.w = pack_bf16x2(v[6], v[7]);
+                    o1.x = pack_bf16x2(v[8], v[9]);
+                    o1.y = pack_bf16x2(v[10], v[11]);
+                    o1.z = pack_bf16x2(v[12], v[13]);
+                    o1.w = pack_bf16x2(v[14], v[15]);
                     dst[0] = o0;
                     dst[1] = o1;
                     ptx::fence_proxy_async_smem();

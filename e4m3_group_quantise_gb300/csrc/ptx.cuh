@@ -69,9 +69,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity, ui
 // the device error word so the host can see what happened.
 constexpr uint32_t SUSPEND_NS = 200000;   // re-check abort / timeout every 0.2 ms at most
 
+// Non-blocking probe of the phase with parity `parity` (about 20 cycles when
+// the phase has already completed, against about 55 for a suspending try_wait).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
                                           uint32_t *err_word, uint32_t code, uint64_t timeout_ns)
 {
+    if (mbar_test_wait(bar, parity))
+        return true;
     if (mbar_try_wait(bar, parity, SUSPEND_NS))
         return true;
     const uint64_t t0 = globaltimer();
@@ -308,6 +325,12 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32])
                    "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
                  :
                  : "memory");
+}
+
+// Waits for every tcgen05.ld of this thread (registers already consumed or discarded).
+__device__ __forceinline__ void tmem_ld_wait_all()
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
 // Shared-memory matrix descriptor for a K-major operand tile stored with the

@@ -6,6 +6,9 @@ softmax, no positional encoding) -> O -> residual -> RMSNorm -> gate_up
 (2 x 1536) -> SiLU(gate) * up -> down -> residual.  Then a final RMSNorm and
 the LM head [vocab 4096, hidden 512].  Weights ~ N(0, 0.02), seed 0.
 The non-linear ops use plain PyTorch (they are not on the FP8 GEMM path).
+``forward(tokens, bf16_linears=True)`` runs every linear layer as a plain
+PyTorch bf16 matmul on the same master weights instead: the BF16 reference
+whose mismatch against the FP8 path the pages describe.
 """
 import torch
 
@@ -41,19 +44,22 @@ class ToyDecoder(torch.nn.Module):
                 if isinstance(m, FP8Linear):
                     m.weight.copy_((torch.randn(m.weight.shape, generator=g) * 0.02).to(torch.bfloat16))
 
-    def forward(self, tokens):
+    def forward(self, tokens, bf16_linears: bool = False):
+        def lin(m, x):
+            return torch.nn.functional.linear(x, m.weight) if bf16_linears else m(x)
+
         B, T = tokens.shape
         h = self.embed[tokens]                                  # [B, T, H] bf16
         mask = torch.ones(T, T, dtype=torch.bool, device=tokens.device).tril()
         for lyr in self.layers:
-            a = lyr.qkv(rmsnorm(h, lyr.n1))                     # [B, T, 3*H]
+            a = lin(lyr.qkv, rmsnorm(h, lyr.n1))                # [B, T, 3*H]
             q, k, v = a.float().view(B, T, 3, HEADS, HEAD_DIM).unbind(2)
             q, k, v = (t.transpose(1, 2) for t in (q, k, v))     # [B, heads, T, d]
             att = (q @ k.transpose(-1, -2)) / HEAD_DIM ** 0.5
             att = att.masked_fill(~mask, float("-inf")).softmax(-1)
             ctx = (att @ v).transpose(1, 2).reshape(B, T, HEADS * HEAD_DIM).to(torch.bfloat16)
-            h = h + lyr.o(ctx)
-            gu = lyr.gate_up(rmsnorm(h, lyr.n2)).float()
+            h = h + lin(lyr.o, ctx)
+            gu = lin(lyr.gate_up, rmsnorm(h, lyr.n2)).float()
             gate, up = gu.chunk(2, dim=-1)
-            h = h + lyr.down((torch.nn.functional.silu(gate) * up).to(torch.bfloat16))
-        return self.head(rmsnorm(h, self.norm))                 # logits [B, T, V] bf16
+            h = h + lin(lyr.down, (torch.nn.functional.silu(gate) * up).to(torch.bfloat16))
+        return lin(self.head, rmsnorm(h, self.norm))            # logits [B, T, V] bf16

@@ -21,6 +21,11 @@ What it computes (Jet-RL technical summaries, gist.science fr/pt,
                                  optional transposed codes.
   * ``gemm_fprop/dgrad/wgrad``  exact fp64 sums of dequantised products,
                                  plus the sum of |products| for tolerances.
+  * ``rmsnorm``, ``swiglu``     the bf16 producers fused in front of the
+                                 linear layers ("Implémentation": fused
+                                 activation / RMSNorm kernels), defined step
+                                 by step in fp32 in the C file; their FP8
+                                 form is ``quantize_act`` of the result.
 Readings the pages leave open (format E4M3-FN, s = amax/448 in fp32, RNE,
 saturating, zero group -> s = 0 and codes 0) are stated in the C file.
 
@@ -81,6 +86,12 @@ def _load():
     lib.jo_quantize_weight.argtypes = [P, I, I, P, P, P]
     for name in ("jo_gemm_fprop", "jo_gemm_dgrad", "jo_gemm_wgrad"):
         getattr(lib, name).argtypes = [P, P, P, P, I, I, I, P, P, I, P, P]
+    lib.jo_exp.restype = ctypes.c_float
+    lib.jo_exp.argtypes = [ctypes.c_float]
+    lib.jo_exp_array.argtypes = [P, I, P]
+    lib.jo_float_to_bf16_array.argtypes = [P, I, P]
+    lib.jo_swiglu.argtypes = [P, I, I, P]
+    lib.jo_rmsnorm.argtypes = [P, P, ctypes.c_float, I, I, P]
     _lib = lib
     return lib
 
@@ -312,3 +323,76 @@ def gemm_within_tolerance(got, ref, abssum, rel: float = 1e-3):
     worst = int(np.nanargmax(np.where(np.isnan(ratio), np.inf, ratio)))
     ok = bool(np.all(np.isfinite(got)) and np.all(ratio <= 1.0))
     return ok, float(ratio.ravel()[worst]), worst
+
+
+# ------------------------------------------------------------ producers
+def exp_f32(x) -> np.ndarray:
+    """The oracle's fp32 e^x (Cody-Waite reduction + degree-7 Taylor)."""
+    lib = _load()
+    v = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(v.shape, dtype=np.float32)
+    lib.jo_exp_array(_ptr(v), v.size, _ptr(out))
+    return out
+
+
+def float_to_bf16_bits(x) -> np.ndarray:
+    """fp32 -> bf16 bit patterns, round to nearest even."""
+    lib = _load()
+    v = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(v.shape, dtype=np.uint16)
+    lib.jo_float_to_bf16_array(_ptr(v), v.size, _ptr(out))
+    return out
+
+
+def swiglu(gu, threads: int = 1) -> np.ndarray:
+    """gate_up output bf16 [M, 2I] -> y bf16 bits [M, I] = silu(gate) * up."""
+    lib = _load()
+    g = _as_bf16_bits(gu)
+    M, I2 = g.shape
+    if I2 % 2:
+        raise ValueError("gate_up width must be even")
+    I = I2 // 2
+    y = np.empty((M, I), dtype=np.uint16)
+
+    def work(r):
+        a, b = r
+        sub = np.ascontiguousarray(g[a:b])
+        out = np.empty((b - a, I), dtype=np.uint16)
+        lib.jo_swiglu(_ptr(sub), b - a, I, _ptr(out))
+        y[a:b] = out
+
+    chunks = _row_chunks(M, max(1, threads)) if M else []
+    if threads <= 1:
+        for c in chunks:
+            work(c)
+    else:
+        with ThreadPoolExecutor(threads) as ex:
+            list(ex.map(work, chunks))
+    return y
+
+
+def rmsnorm(x, gamma, eps: float, threads: int = 1) -> np.ndarray:
+    """x bf16 [M, H], gamma bf16 [H] -> y bf16 bits [M, H] (H % 256 == 0)."""
+    lib = _load()
+    xb = _as_bf16_bits(x)
+    gb = np.ascontiguousarray(_as_bf16_bits(gamma).reshape(-1))
+    M, H = xb.shape
+    if H % 256 or gb.size != H:
+        raise ValueError("H must be a multiple of 256 and gamma must have H entries")
+    y = np.empty((M, H), dtype=np.uint16)
+
+    def work(r):
+        a, b = r
+        sub = np.ascontiguousarray(xb[a:b])
+        out = np.empty((b - a, H), dtype=np.uint16)
+        lib.jo_rmsnorm(_ptr(sub), _ptr(gb), ctypes.c_float(eps), b - a, H, _ptr(out))
+        y[a:b] = out
+
+    chunks = _row_chunks(M, max(1, threads)) if M else []
+    if threads <= 1:
+        for c in chunks:
+            work(c)
+    else:
+        with ThreadPoolExecutor(threads) as ex:
+            list(ex.map(work, chunks))
+    return y

@@ -298,7 +298,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
     ap.add_argument("--case", default=None,
                     help="time one kernel alone, e.g. fprop:16384x6144x4096 (KIND:MxNxK; KIND in fprop, dgrad, "
-                         "wgrad, quant_x, quant_xt, quant_dual, quant_w) -- a single-kernel line for profiling, not the metric")
+                         "wgrad, quant_x, quant_xt, quant_dual, quant_w, rmsnorm_q, swiglu_q) -- a single-kernel line for profiling, "
+                         "not the metric")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -408,6 +409,15 @@ def run_case(args):
         else:
             q, s = torch.empty(K, M, dtype=torch.uint8, device=dev), torch.empty(M // 128, K, device=dev)
             fn = lambda: jf.jetfp8_quantize_act_transposed(x, q, s)  # noqa: E731
+    elif kind == "rmsnorm_q":          # M x 0 x H: RMSNorm fused with the 1x128 quantiser
+        x = syn.activation(M, K, seed=1, outlier_scale=20.0, device=dev)
+        gamma = torch.ones(K, dtype=torch.bfloat16, device=dev)
+        q, s = torch.empty(M, K, dtype=torch.uint8, device=dev), torch.empty(K // 128, M, device=dev)
+        fn = lambda: jf.jetfp8_rmsnorm_quantize_act(x, gamma, 1e-6, q, s)  # noqa: E731
+    elif kind == "swiglu_q":           # M x 0 x I: SwiGLU of [M, 2I] fused with the 1x128 quantiser
+        gu = syn.activation(M, 2 * K, seed=1, device=dev)
+        q, s = torch.empty(M, K, dtype=torch.uint8, device=dev), torch.empty(K // 128, M, device=dev)
+        fn = lambda: jf.jetfp8_swiglu_quantize_act(gu, q, s)  # noqa: E731
     elif kind == "quant_w":
         w = syn.weight(N, K, seed=1, device=dev)
         q, s = torch.empty(N, K, dtype=torch.uint8, device=dev), torch.empty(N // 128, K // 128, device=dev)
@@ -434,6 +444,8 @@ def run_case(args):
             byts = N * K * 4 + 4 * (N // 128) * (K // 128)
         elif kind == "quant_dual":
             byts = M * K * (4 + 8 / 128)
+        elif kind == "swiglu_q":
+            byts = M * K * (5 + 4 / 128)
         else:
             byts = M * K * (3 + 4 / 128)
         rec["gbs"] = round(byts / (ms * 1e-3) / 1e9, 1)

@@ -16,6 +16,8 @@ from .jetfp8 import (  # noqa: F401
     jetfp8_quantize_act_dual,
     jetfp8_quantize_act_transposed,
     jetfp8_quantize_weight,
+    jetfp8_rmsnorm_quantize_act,
+    jetfp8_swiglu_quantize_act,
     jetfp8_status_string,
     jetfp8_watchdog_selftest,
     load_library,
@@ -23,5 +25,7 @@ from .jetfp8 import (  # noqa: F401
     quantize_act_dual,
     quantize_act_transposed,
     quantize_weight,
+    rmsnorm_quantize_act,
+    swiglu_quantize_act,
 )
 from .linear import FP8Linear, FP8LinearFunction, QuantizedWeight  # noqa: F401

@@ -19,8 +19,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libjetfp8.so")
-SOURCES = ["api.cu", "quantize.cu", "gemm.cu"]
-HEADERS = ["ptx.cuh", "internal.cuh"]
+SOURCES = ["api.cu", "quantize.cu", "gemm.cu", "producers.cu"]
+HEADERS = ["ptx.cuh", "internal.cuh", "e4m3.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # IEEE division and denormals are part of the numerical contract: no

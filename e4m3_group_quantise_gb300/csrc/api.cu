@@ -257,6 +257,56 @@ JETFP8_API jetfp8_status jetfp8_quantize_weight(const void *w, int64_t N, int64_
     return launch_status(jetfp8::launch_quantize_weight(w, N, K, q, s, qt, static_cast<cudaStream_t>(stream)));
 }
 
+JETFP8_API jetfp8_status jetfp8_rmsnorm_quantize_act(const void *x, const void *gamma, float eps, int64_t M,
+                                                     int64_t H, uint8_t *q, float *s, void *y, void *stream)
+{
+    if (M < 0 || H <= 0 || H % 256 != 0 || !dims_ok(M, H) || (M + 7) / 8 > 0x7fffffff)
+        return JETFP8_ERR_SHAPE;
+    if (!(eps >= 0.0f) || eps > 3.4e38f)                 // NaN, negative and infinite eps rejected
+        return JETFP8_ERR_INVALID_VALUE;
+    if (M == 0)
+        return JETFP8_OK;
+    if (!x || !gamma || (q == nullptr) != (s == nullptr) || (!q && !y))
+        return JETFP8_ERR_INVALID_VALUE;
+    if (!aligned16(x) || !aligned16(gamma) || (q && (!aligned16(q) || !aligned16(s))) || (y && !aligned16(y)))
+        return JETFP8_ERR_ALIGNMENT;
+    const Range outs[3] = {range_of(q, q ? M * H : 0), range_of(s, s ? M * (H / 128) * 4 : 0),
+                           range_of(y, y ? M * H * 2 : 0)};
+    const Range ins[2] = {range_of(x, M * H * 2), range_of(gamma, H * 2)};
+    if (any_overlap(outs, 3, ins, 2))
+        return JETFP8_ERR_INVALID_VALUE;
+    const DeviceInfo *dev = nullptr;
+    jetfp8_status st = current_device(&dev);
+    if (st != JETFP8_OK)
+        return st;
+    return launch_status(
+        jetfp8::launch_rmsnorm_quantize(x, gamma, eps, M, H, q, s, y, static_cast<cudaStream_t>(stream)));
+}
+
+JETFP8_API jetfp8_status jetfp8_swiglu_quantize_act(const void *gu, int64_t M, int64_t I, uint8_t *q, float *s,
+                                                    void *y, void *stream)
+{
+    if (M < 0 || I <= 0 || I % 256 != 0 || !dims_ok(M, 2 * I))
+        return JETFP8_ERR_SHAPE;
+    if (M == 0)
+        return JETFP8_OK;
+    if (!gu || (q == nullptr) != (s == nullptr) || (!q && !y))
+        return JETFP8_ERR_INVALID_VALUE;
+    if (!aligned16(gu) || (q && (!aligned16(q) || !aligned16(s))) || (y && !aligned16(y)))
+        return JETFP8_ERR_ALIGNMENT;
+    const Range outs[3] = {range_of(q, q ? M * I : 0), range_of(s, s ? M * (I / 128) * 4 : 0),
+                           range_of(y, y ? M * I * 2 : 0)};
+    const Range ins[1] = {range_of(gu, M * I * 4)};
+    if (any_overlap(outs, 3, ins, 1))
+        return JETFP8_ERR_INVALID_VALUE;
+    const DeviceInfo *dev = nullptr;
+    jetfp8_status st = current_device(&dev);
+    if (st != JETFP8_OK)
+        return st;
+    return launch_status(jetfp8::launch_swiglu_quantize(gu, M, I, q, s, y, dev->sm_count,
+                                                        static_cast<cudaStream_t>(stream)));
+}
+
 JETFP8_API jetfp8_status jetfp8_gemm_fprop(const uint8_t *qx, const float *sx, const uint8_t *qw, const float *sw,
                                            void *y, int64_t M, int64_t N, int64_t K, void *stream)
 {

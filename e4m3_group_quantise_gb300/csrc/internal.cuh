@@ -29,6 +29,13 @@ cudaError_t launch_quantize_act_dual(const void *x, int64_t M, int64_t K, uint8_
 cudaError_t launch_quantize_weight(const void *w, int64_t N, int64_t K, uint8_t *q, float *s, uint8_t *qt,
                                    cudaStream_t stream);
 
+// Fused producers (producers.cu): RMSNorm / SwiGLU -> bf16 -> 1x128 FP8.
+// q and s may be null (then only y is written); y may be null.
+cudaError_t launch_rmsnorm_quantize(const void *x, const void *gamma, float eps, int64_t M, int64_t H, uint8_t *q,
+                                    float *s, void *y, cudaStream_t stream);
+cudaError_t launch_swiglu_quantize(const void *gu, int64_t M, int64_t I, uint8_t *q, float *s, void *y,
+                                   int sm_count, cudaStream_t stream);
+
 // One block-scaled GEMM D[rows][cols] = sum_g sa(g,row) sb(g,col) (A_g B_g^T),
 // A: [rows][kdim] codes, B: [cols][kdim] codes, both K-major (gemm.cu).
 enum class ScaleB { PerBlock128, PerColumn };

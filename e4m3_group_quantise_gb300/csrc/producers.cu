@@ -1,0 +1,216 @@
+// Producers fused in front of the FP8 linear layers: RMSNorm and SwiGLU that
+// emit the next GEMM's 1x128 FP8 input directly (Jet-RL technical summaries,
+// "Implémentation": fused activation / RMSNorm kernels feeding the FP8
+// GEMMs), so the bf16 intermediate need not make a round trip through HBM.
+//
+// The pages give no arithmetic for these operators; this library defines it
+// step by step: every operation below is one IEEE fp32 operation in a fixed
+// order (written with the _rn intrinsics and fmaf, so the compiler never
+// contracts a multiply and an add), the result is rounded to bf16 (nearest
+// even), and that bf16 value is quantised exactly as jetfp8_quantize_act
+// quantises it.  The optional bf16 output is the same rounded value.
+//
+// Layout of the work: a warp takes a 256-column chunk of one row, lane l the
+// eight values 8l .. 8l+7, loaded and stored as 16-byte vectors.  A 1x128
+// group is then one half-warp: its amax takes four shuffles and its codes
+// leave as one contiguous 128-byte store.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "e4m3.cuh"
+#include "internal.cuh"
+
+namespace jetfp8 {
+namespace {
+
+constexpr int PR_THREADS = 256;
+constexpr int PR_WARPS = PR_THREADS / 32;
+
+__device__ __forceinline__ float pow2_normal(int k)   // 2^k, -126 <= k <= 127
+{
+    return __int_as_float((k + 127) << 23);
+}
+
+// e^x in fp32: Cody-Waite range reduction x = n ln2 + r with
+// n = rint(x / ln2), |r| <= ln2 / 2; e^r from its degree-7 Taylor polynomial
+// in Horner form with fused multiply-adds; then the scaling by 2^n in two
+// exact steps.  ln2 is split into a head with 16 significant bits (45426 /
+// 2^16, so n * head is exact) and the rounded remainder.  x >= 89 gives
+// +inf, x < -87 gives +0.
+__device__ __forceinline__ float exp_f32(float x)
+{
+    if (x != x)
+        return x;
+    if (x >= 89.0f)
+        return __int_as_float(0x7f800000);
+    if (x < -87.0f)
+        return 0.0f;
+    const float n = rintf(__fmul_rn(x, 1.44269502f));   // fp32(1 / ln 2)
+    float r = fmaf(-n, 0.693145751953125f, x);           // 45426 / 65536
+    r = fmaf(-n, 1.42860677e-06f, r);                    // fp32(ln 2 - 45426 / 65536)
+    float p = 0.000198412701f;                           // fp32(1 / k!), k = 7 .. 2
+    p = fmaf(p, r, 0.00138888892f);
+    p = fmaf(p, r, 0.00833333377f);
+    p = fmaf(p, r, 0.0416666679f);
+    p = fmaf(p, r, 0.166666672f);
+    p = fmaf(p, r, 0.5f);
+    p = fmaf(p, r, 1.0f);
+    p = fmaf(p, r, 1.0f);
+    const int ni = static_cast<int>(n);                  // -126 .. 128
+    const int n1 = ni / 2;
+    return __fmul_rn(__fmul_rn(p, pow2_normal(n1)), pow2_normal(ni - n1));
+}
+
+__device__ __forceinline__ float round_bf16(float v)
+{
+    return __bfloat162float(__float2bfloat16_rn(v));
+}
+
+__device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi)
+{
+    // both values are already bf16-exact: the conversion only moves bits
+    return (__float_as_uint(lo) >> 16) | (__float_as_uint(hi) & 0xFFFF0000u);
+}
+
+// The eight bf16-exact values v of this lane belong to the 1x128 group of
+// its half-warp: group amax, scale, codes (written at q8) and, from the
+// half-warp's first lane, the scale (written at *scale).
+__device__ __forceinline__ void quantize8_halfwarp(const float (&v)[8], uint8_t *q8, float *scale, int lane)
+{
+    float amax = 0.0f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        amax = fmaxf(amax, fabsf(v[e]));
+#pragma unroll
+    for (int d = 8; d >= 1; d >>= 1)
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+    const GroupScale gs = group_scale(amax);
+    uint32_t w[2];
+    const uint32_t redo = encode_words<2>(v, gs, w);
+    // rare: a word whose bracket disagreed takes the exact quotient
+    if (redo & 1u)
+        w[0] = encode4_exact(v[0], v[1], v[2], v[3], gs.s);
+    if (redo & 2u)
+        w[1] = encode4_exact(v[4], v[5], v[6], v[7], gs.s);
+    *reinterpret_cast<uint2 *>(q8) = make_uint2(w[0], w[1]);
+    if ((lane & 15) == 0)
+        *scale = gs.s;
+}
+
+// ---------------------------------------------------------------------------
+// RMSNorm: one warp per row.  Pass 1 sums the squares: lane l adds, in order,
+// the squares of its chunks' values (chunk 32 j + l, j = 0, 1, ...), then the
+// lanes combine by butterfly (partner distance 16, 8, 4, 2, 1).  Pass 2
+// re-reads the row (from cache), forms y = bf16((x * rstd) * gamma) and
+// quantises it.  Both passes are unrolled four chunks deep so that each warp
+// keeps several loads in flight; the additions stay in chunk order.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float sum_squares8(float acc, const uint4 &c)
+{
+    float f[8];
+    unpack8(c, f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        acc = __fadd_rn(acc, __fmul_rn(f[e], f[e]));
+    return acc;
+}
+
+__global__ void __launch_bounds__(PR_THREADS)
+rmsnorm_quantize_kernel(const uint4 *__restrict__ x, const uint4 *__restrict__ gamma, float eps, int64_t M,
+                        int64_t H, uint8_t *__restrict__ q, float *__restrict__ s, uint4 *__restrict__ y)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * PR_WARPS + (threadIdx.x >> 5);
+    if (row >= M)
+        return;                                   // whole warps only
+    const int64_t H8 = H >> 3;
+    const uint4 *xr = x + row * H8;
+    const int nj = static_cast<int>(H >> 8);
+
+    float acc = 0.0f;
+#pragma unroll 4
+    for (int j = 0; j < nj; ++j)
+        acc = sum_squares8(acc, __ldg(xr + 32 * j + lane));
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1)
+        acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, d));
+    const float ms = __fdiv_rn(acc, static_cast<float>(H));
+    const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+
+#pragma unroll 4
+    for (int j = 0; j < nj; ++j) {
+        const int64_t c = 32 * j + lane;
+        float f[8], g[8], v[8];
+        unpack8(__ldg(xr + c), f);
+        unpack8(__ldg(gamma + c), g);
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            v[e] = round_bf16(__fmul_rn(__fmul_rn(f[e], rstd), g[e]));
+        if (y)
+            y[row * H8 + c] = make_uint4(pack2_bf16(v[0], v[1]), pack2_bf16(v[2], v[3]), pack2_bf16(v[4], v[5]),
+                                         pack2_bf16(v[6], v[7]));
+        if (q)
+            quantize8_halfwarp(v, q + row * H + 8 * c, s + (c >> 4) * M + row, lane);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// SwiGLU of a gate_up output [M][2I] (gate = columns 0..I-1, up = I..2I-1):
+// y = bf16( (g * (1 / (1 + e^-g))) * u ).  A warp handles one 256-column
+// chunk of one row per iteration (grid-stride over all chunks).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(PR_THREADS)
+swiglu_quantize_kernel(const uint4 *__restrict__ gu, int64_t M, int64_t I, uint8_t *__restrict__ q,
+                       float *__restrict__ s, uint4 *__restrict__ y)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t chunks = I >> 8;
+    const int64_t items = M * chunks;
+    const int64_t in_row = I >> 2;                // uint4 per gate_up row (2I bf16)
+    const int64_t out_row = I >> 3;               // uint4 per output row
+    for (int64_t it = static_cast<int64_t>(blockIdx.x) * PR_WARPS + (threadIdx.x >> 5); it < items;
+         it += static_cast<int64_t>(gridDim.x) * PR_WARPS) {
+        const int64_t row = it / chunks;
+        const int64_t c = (it - row * chunks) * 32 + lane;   // output uint4 index within the row
+        float g[8], u[8], v[8];
+        unpack8(__ldg(gu + row * in_row + c), g);
+        unpack8(__ldg(gu + row * in_row + out_row + c), u);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            // 1 / (1 + e^-g): the correctly rounded reciprocal is the IEEE quotient
+            const float sig = __frcp_rn(__fadd_rn(1.0f, exp_f32(-g[e])));
+            v[e] = round_bf16(__fmul_rn(__fmul_rn(g[e], sig), u[e]));
+        }
+        if (y)
+            y[row * out_row + c] = make_uint4(pack2_bf16(v[0], v[1]), pack2_bf16(v[2], v[3]),
+                                              pack2_bf16(v[4], v[5]), pack2_bf16(v[6], v[7]));
+        if (q)
+            quantize8_halfwarp(v, q + row * I + 8 * c, s + (c >> 4) * M + row, lane);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_rmsnorm_quantize(const void *x, const void *gamma, float eps, int64_t M, int64_t H, uint8_t *q,
+                                    float *s, void *y, cudaStream_t stream)
+{
+    const int64_t blocks = (M + PR_WARPS - 1) / PR_WARPS;
+    rmsnorm_quantize_kernel<<<static_cast<unsigned>(blocks), PR_THREADS, 0, stream>>>(
+        static_cast<const uint4 *>(x), static_cast<const uint4 *>(gamma), eps, M, H, q, s, static_cast<uint4 *>(y));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_swiglu_quantize(const void *gu, int64_t M, int64_t I, uint8_t *q, float *s, void *y,
+                                   int sm_count, cudaStream_t stream)
+{
+    const int64_t items = M * (I >> 8);
+    const int64_t want = (items + PR_WARPS - 1) / PR_WARPS;
+    const int64_t cap = static_cast<int64_t>(sm_count) * 8;    // 8 resident blocks per SM
+    const int64_t blocks = want < cap ? want : cap;
+    swiglu_quantize_kernel<<<static_cast<unsigned>(blocks), PR_THREADS, 0, stream>>>(
+        static_cast<const uint4 *>(gu), M, I, q, s, static_cast<uint4 *>(y));
+    return cudaGetLastError();
+}
+
+}  // namespace jetfp8

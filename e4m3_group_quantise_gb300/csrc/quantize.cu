@@ -12,111 +12,17 @@
 // amax reductions, and stores arranged so that every written sector is full.
 // Compiled without fast-math so that `/` is the correctly rounded IEEE
 // division and subnormals are kept; the per-element division itself is
-// replaced by an exact bracketing test (see encode2), with the division as the
+// replaced by an exact bracketing test (e4m3.cuh), with the division as the
 // rare fallback.
 #include <cuda_runtime.h>
 #include <cstdint>
 
+#include "e4m3.cuh"
 #include "internal.cuh"
 #include "ptx.cuh"
 
 namespace jetfp8 {
 namespace {
-
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-__device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8])
-{
-    f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
-    f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
-    f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z);
-    f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
-}
-
-__device__ __forceinline__ float absmax8(const float (&f)[8])
-{
-    float a = fabsf(f[0]);
-#pragma unroll
-    for (int i = 1; i < 8; ++i)
-        a = fmaxf(a, fabsf(f[i]));
-    return a;
-}
-
-// Exact E4M3 codes of fp32(x / s) without a division per element.
-//
-// With r = RN(1/s) (IEEE reciprocal), ra = RN(r (1 - 2^-21)) and
-// rb = RN(r (1 + 2^-21)), the products va = RN(x ra) and vb = RN(x rb) satisfy
-// |va| < |x/s| < |vb| (same sign): each carries at most three roundings of
-// relative size 2^-24, which the 2^-21 margin outweighs.  Round-to-nearest-even
-// with saturation is monotone, so every fp32 value between va and vb -- in
-// particular fp32(x/s) -- has the same E4M3 code whenever va and vb do.  Only
-// when they differ (x/s within ~2^-21 of a rounding midpoint, or exactly on
-// one) is the correctly rounded quotient x / s computed.  A subnormal scale
-// (1/s would overflow) always takes the division.
-struct GroupScale {
-    float s, ra, rb;
-    bool fast;
-};
-
-__device__ __forceinline__ GroupScale group_scale(float amax)
-{
-    GroupScale g;
-    g.s = amax / 448.0f;
-    g.fast = g.s >= 1.17549435e-38f;        // smallest normal fp32
-    const float r = __frcp_rn(g.fast ? g.s : 1.0f);
-    g.ra = r * 0x1.fffffp-1f;              // 1 - 2^-21
-    g.rb = r * 0x1.000008p+0f;             // 1 + 2^-21
-    return g;
-}
-
-// Codes of 4N consecutive values into N little-endian words (value i in
-// byte i of its word), from the lower bracket end, two values per packed
-// multiply.  Returns a mask with bit k set when word k needs the exact
-// quotient (some value's bracket ends disagree, or the scale is subnormal);
-// the caller recomputes those words with encode4_exact from a re-read of the
-// input.  A zero scale (all-zero group) gives zero codes and no work.
-// On normal-distributed bf16 data about 0.5 % of the values sit on or next to
-// a rounding midpoint (x / amax is a short binary fraction), so patching only
-// the flagged words keeps the exact path off the common path.
-template <int N>
-__device__ __forceinline__ uint32_t encode_words(const float *f, const GroupScale &g, uint32_t *w)
-{
-    static_assert(N <= 32, "one mask bit per word");
-    if (g.s == 0.0f || !g.fast) {
-#pragma unroll
-        for (int k = 0; k < N; ++k)
-            w[k] = 0u;
-        return g.s == 0.0f ? 0u : (N == 32 ? 0xffffffffu : ((1u << N) - 1u));
-    }
-    const uint64_t ra2 = ptx::pack_f32x2(g.ra, g.ra), rb2 = ptx::pack_f32x2(g.rb, g.rb);
-    uint32_t mask = 0u;
-#pragma unroll
-    for (int k = 0; k < N; ++k) {
-        const uint64_t x0 = ptx::pack_f32x2(f[4 * k], f[4 * k + 1]);
-        const uint64_t x1 = ptx::pack_f32x2(f[4 * k + 2], f[4 * k + 3]);
-        const uint64_t a0 = ptx::mul_f32x2(x0, ra2), b0 = ptx::mul_f32x2(x0, rb2);
-        const uint64_t a1 = ptx::mul_f32x2(x1, ra2), b1 = ptx::mul_f32x2(x1, rb2);
-        const uint32_t lo = ptx::cvt_e4m3x2(ptx::lo_f32(a0), ptx::hi_f32(a0)) |
-                            (ptx::cvt_e4m3x2(ptx::lo_f32(a1), ptx::hi_f32(a1)) << 16);
-        const uint32_t hi = ptx::cvt_e4m3x2(ptx::lo_f32(b0), ptx::hi_f32(b0)) |
-                            (ptx::cvt_e4m3x2(ptx::lo_f32(b1), ptx::hi_f32(b1)) << 16);
-        w[k] = lo;
-        mask |= (lo != hi ? 1u : 0u) << k;
-    }
-    return mask;
-}
-
-// Codes of four values through the correctly rounded quotient x / s.
-__device__ __forceinline__ uint32_t encode4_exact(float a, float b, float c, float d, float s)
-{
-    return ptx::cvt_e4m3x2(a / s, b / s) | (ptx::cvt_e4m3x2(c / s, d / s) << 16);
-}
-
-__device__ __forceinline__ uint32_t encode4_exact(uint2 bf16x4, float s)
-{
-    return encode4_exact(bf16_lo(bf16x4.x), bf16_hi(bf16x4.x), bf16_lo(bf16x4.y), bf16_hi(bf16x4.y), s);
-}
 
 // ---------------------------------------------------------------------------
 // 1x128 groups along rows.  CTA tile: 16 rows x 8 groups (1024 columns).

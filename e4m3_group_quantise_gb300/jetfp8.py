@@ -60,10 +60,12 @@ def load_library():
     lib.jetfp8_quantize_act_transposed.argtypes = [P, I, I, P, P, P]
     lib.jetfp8_quantize_weight.argtypes = [P, I, I, P, P, P, P]
     lib.jetfp8_quantize_act_dual.argtypes = [P, I, I, P, P, P, P, P]
+    lib.jetfp8_rmsnorm_quantize_act.argtypes = [P, P, ctypes.c_float, I, I, P, P, P, P]
+    lib.jetfp8_swiglu_quantize_act.argtypes = [P, I, I, P, P, P, P]
     for name in ("jetfp8_gemm_fprop", "jetfp8_gemm_dgrad", "jetfp8_gemm_wgrad"):
         getattr(lib, name).argtypes = [P, P, P, P, P, I, I, I, P]
     for name in ("jetfp8_quantize_act", "jetfp8_quantize_act_transposed", "jetfp8_quantize_weight",
-                 "jetfp8_quantize_act_dual",
+                 "jetfp8_quantize_act_dual", "jetfp8_rmsnorm_quantize_act", "jetfp8_swiglu_quantize_act",
                  "jetfp8_gemm_fprop", "jetfp8_gemm_dgrad", "jetfp8_gemm_wgrad"):
         getattr(lib, name).restype = S
     lib.jetfp8_act_scale_count.argtypes = [I, I]
@@ -147,6 +149,32 @@ def jetfp8_quantize_act_dual(x, q, s, qt, st, stream=None):
     _want(st, torch.float32, (M // 128, K), "st")
     _check(load_library().jetfp8_quantize_act_dual(_ptr(x), M, K, _ptr(q), _ptr(s), _ptr(qt), _ptr(st),
                                                    _stream(stream)), "jetfp8_quantize_act_dual")
+
+
+def jetfp8_rmsnorm_quantize_act(x, gamma, eps, q, s, y=None, stream=None):
+    M, H = x.shape
+    _want(x, torch.bfloat16, (M, H), "x")
+    _want(gamma, torch.bfloat16, (H,), "gamma")
+    if q is not None or s is not None:
+        _want(q, torch.uint8, (M, H), "q")
+        _want(s, torch.float32, (H // 128, M), "s")
+    if y is not None:
+        _want(y, torch.bfloat16, (M, H), "y")
+    _check(load_library().jetfp8_rmsnorm_quantize_act(_ptr(x), _ptr(gamma), float(eps), M, H, _ptr(q), _ptr(s),
+                                                      _ptr(y), _stream(stream)), "jetfp8_rmsnorm_quantize_act")
+
+
+def jetfp8_swiglu_quantize_act(gu, q, s, y=None, stream=None):
+    M, I2 = gu.shape
+    I = I2 // 2
+    _want(gu, torch.bfloat16, (M, 2 * I), "gu")
+    if q is not None or s is not None:
+        _want(q, torch.uint8, (M, I), "q")
+        _want(s, torch.float32, (I // 128, M), "s")
+    if y is not None:
+        _want(y, torch.bfloat16, (M, I), "y")
+    _check(load_library().jetfp8_swiglu_quantize_act(_ptr(gu), M, I, _ptr(q), _ptr(s), _ptr(y), _stream(stream)),
+           "jetfp8_swiglu_quantize_act")
 
 
 def jetfp8_quantize_weight(w, q, s, qt=None, stream=None):
@@ -241,6 +269,29 @@ def quantize_act_dual(x: torch.Tensor, stream=None):
     st = torch.empty((M // 128, K), dtype=torch.float32, device=x.device)
     jetfp8_quantize_act_dual(x, q, s, qt, st, stream)
     return q, s, qt, st
+
+
+def rmsnorm_quantize_act(x: torch.Tensor, gamma: torch.Tensor, eps: float, quantize: bool = True,
+                         want_y: bool = False, stream=None):
+    """RMSNorm fused with the 1x128 quantiser: (q, s, y) with y None unless
+    ``want_y``; ``quantize=False`` gives only y (q and s None)."""
+    M, H = x.shape
+    q = torch.empty((M, H), dtype=torch.uint8, device=x.device) if quantize else None
+    s = torch.empty((H // 128, M), dtype=torch.float32, device=x.device) if quantize else None
+    y = torch.empty((M, H), dtype=torch.bfloat16, device=x.device) if want_y or not quantize else None
+    jetfp8_rmsnorm_quantize_act(x, gamma, eps, q, s, y, stream)
+    return q, s, y
+
+
+def swiglu_quantize_act(gu: torch.Tensor, quantize: bool = True, want_y: bool = False, stream=None):
+    """SwiGLU of a gate_up output [M, 2I] fused with the 1x128 quantiser:
+    (q, s, y) as for ``rmsnorm_quantize_act``."""
+    M, I = gu.shape[0], gu.shape[1] // 2
+    q = torch.empty((M, I), dtype=torch.uint8, device=gu.device) if quantize else None
+    s = torch.empty((I // 128, M), dtype=torch.float32, device=gu.device) if quantize else None
+    y = torch.empty((M, I), dtype=torch.bfloat16, device=gu.device) if want_y or not quantize else None
+    jetfp8_swiglu_quantize_act(gu, q, s, y, stream)
+    return q, s, y
 
 
 def quantize_weight(w: torch.Tensor, transposed: bool = True, stream=None):

@@ -97,3 +97,11 @@ class FP8Linear(torch.nn.Module):
             qx, sx = _j.quantize_act(x2d)
             y = _j.gemm_fprop(qx, sx, q, s)
         return y.reshape(*shape[:-1], y.shape[-1])
+
+    def forward_quantized(self, qx: torch.Tensor, sx: torch.Tensor) -> torch.Tensor:
+        """Rollout Fprop on an input that is already FP8 (1x128 codes qx
+        [M, in], scales sx [in/128, M]), e.g. from a fused RMSNorm or SwiGLU
+        producer; no autograd.  Bit-identical to ``forward`` on the bf16 value
+        those codes quantise."""
+        q, s, _ = self._cache.get(self.weight)
+        return _j.gemm_fprop(qx, sx, q, s)

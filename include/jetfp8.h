@@ -115,6 +115,45 @@ JETFP8_API jetfp8_status jetfp8_quantize_act_dual(const void *x, int64_t M, int6
                                                   uint8_t *qt, float *st, void *stream);
 
 /*
+ * Fused RMSNorm producer: the 1x128 FP8 input of the next linear layer
+ * straight from the residual stream (Jet-RL, "Implémentation": fused
+ * activation / RMSNorm kernels in front of the FP8 GEMMs).  Per row:
+ *   ms = (sum of x_i^2) / H, rstd = 1 / sqrt(ms + eps),
+ *   y_i = bf16((x_i * rstd) * gamma_i)   (round to nearest even),
+ * each step one IEEE fp32 operation; the sum of squares runs in a fixed
+ * order (32 partial sums, partial l over the 8-element chunks 32 j + l in
+ * increasing j, combined pairwise at distances 16, 8, 4, 2, 1).  The codes
+ * and scales are exactly those jetfp8_quantize_act gives for y.
+ *   x     : bf16 [M][H]                    (input)
+ *   gamma : bf16 [H]                       (input)
+ *   eps   : finite, >= 0
+ *   q, s  : uint8 [M][H], fp32 [H/128][M]  (as jetfp8_quantize_act), or both NULL
+ *   y     : bf16 [M][H] or NULL            (the normalised values themselves)
+ * At least one of (q, s) and y is given.  Requires H > 0, H % 256 == 0,
+ * M * H < 2^40.
+ */
+JETFP8_API jetfp8_status jetfp8_rmsnorm_quantize_act(const void *x, const void *gamma, float eps, int64_t M,
+                                                     int64_t H, uint8_t *q, float *s, void *y, void *stream);
+
+/*
+ * Fused SwiGLU producer: the 1x128 FP8 input of the down projection from
+ * the gate_up output (Jet-RL, "Implémentation": fused activation kernels).
+ * gu holds gate in columns 0..I-1 and up in columns I..2I-1 of each row;
+ *   y = bf16( (g * (1 / (1 + e^-g))) * u )
+ * with one IEEE fp32 operation per step and e^x this library's own fp32
+ * exponential: Cody-Waite reduction by ln 2 and a degree-7 Taylor
+ * polynomial (within 2 ulp of e^x; +inf for x >= 89, +0 for x < -87).
+ * The codes and scales are exactly those jetfp8_quantize_act gives for y.
+ *   gu   : bf16 [M][2I]                    (input)
+ *   q, s : uint8 [M][I], fp32 [I/128][M], or both NULL
+ *   y    : bf16 [M][I] or NULL
+ * At least one of (q, s) and y is given.  Requires I > 0, I % 256 == 0,
+ * M * 2I < 2^40.
+ */
+JETFP8_API jetfp8_status jetfp8_swiglu_quantize_act(const void *gu, int64_t M, int64_t I, uint8_t *q, float *s,
+                                                    void *y, void *stream);
+
+/*
  * Weight quantisation, 128x128 blocks (Jet-RL, "Schéma de Quantification":
  * weights 128x128 per block; master weights stay BF16, "Architecture
  * Centrale").

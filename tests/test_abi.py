@@ -91,6 +91,35 @@ def test_quantize_weight_validation(lib):
     assert f(A16, 128, 128, B16, C16, B16 + 128, None) == J.ERR_INVALID_VALUE   # qt overlaps q
 
 
+def test_rmsnorm_quantize_validation(lib):
+    f = lib.jetfp8_rmsnorm_quantize_act
+    assert f(A16, B16, 1e-6, 4, 384, C16, D16, None, None) == J.ERR_SHAPE        # H % 256
+    assert f(A16, B16, 1e-6, -1, 512, C16, D16, None, None) == J.ERR_SHAPE
+    assert f(A16, B16, 1e-6, 4, 0, C16, D16, None, None) == J.ERR_SHAPE
+    assert f(None, None, 1e-6, 0, 512, None, None, None, None) == J.OK             # empty
+    assert f(A16, B16, -1.0, 4, 512, C16, D16, None, None) == J.ERR_INVALID_VALUE   # eps < 0
+    assert f(A16, B16, float("nan"), 4, 512, C16, D16, None, None) == J.ERR_INVALID_VALUE
+    assert f(A16, B16, float("inf"), 4, 512, C16, D16, None, None) == J.ERR_INVALID_VALUE
+    assert f(A16, B16, 1e-6, 4, 512, C16, None, None, None) == J.ERR_INVALID_VALUE  # q without s
+    assert f(A16, B16, 1e-6, 4, 512, None, None, None, None) == J.ERR_INVALID_VALUE  # nothing to write
+    assert f(None, B16, 1e-6, 4, 512, C16, D16, None, None) == J.ERR_INVALID_VALUE
+    assert f(A16, B16 + 2, 1e-6, 4, 512, C16, D16, None, None) == J.ERR_ALIGNMENT
+    assert f(A16, B16, 1e-6, 4, 512, None, None, E16 + 8, None) == J.ERR_ALIGNMENT
+    assert f(A16, B16, 1e-6, 4, 512, A16 + 16, D16, None, None) == J.ERR_INVALID_VALUE   # q overlaps x
+    assert f(A16, B16, 1e-6, 4, 512, C16, D16, C16 + 16, None) == J.ERR_INVALID_VALUE    # y overlaps q
+
+
+def test_swiglu_quantize_validation(lib):
+    f = lib.jetfp8_swiglu_quantize_act
+    assert f(A16, 4, 128, C16, D16, None, None) == J.ERR_SHAPE                  # I % 256
+    assert f(A16, 4, 0, C16, D16, None, None) == J.ERR_SHAPE
+    assert f(None, 0, 256, None, None, None, None) == J.OK
+    assert f(A16, 4, 256, None, D16, None, None) == J.ERR_INVALID_VALUE         # s without q
+    assert f(A16, 4, 256, None, None, None, None) == J.ERR_INVALID_VALUE
+    assert f(A16 + 4, 4, 256, C16, D16, None, None) == J.ERR_ALIGNMENT
+    assert f(A16, 4, 256, A16 + 1024, D16, None, None) == J.ERR_INVALID_VALUE    # q inside gu
+
+
 @pytest.mark.parametrize("name", ["jetfp8_gemm_fprop", "jetfp8_gemm_dgrad", "jetfp8_gemm_wgrad"])
 def test_gemm_validation(lib, name):
     f = getattr(lib, name)
@@ -115,6 +144,8 @@ def test_no_device_reported_cleanly(lib):
     assert lib.jetfp8_gemm_fprop(A16, B16, C16, D16, E16, 128, 128, 128, None) == J.ERR_UNSUPPORTED_DEVICE
     assert lib.jetfp8_poll_device_error(None) == J.ERR_UNSUPPORTED_DEVICE
     assert lib.jetfp8_watchdog_selftest(0, None) == J.ERR_SHAPE
+    assert lib.jetfp8_rmsnorm_quantize_act(A16, B16, 1e-6, 4, 512, C16, D16, None, None) == J.ERR_UNSUPPORTED_DEVICE
+    assert lib.jetfp8_swiglu_quantize_act(A16, 4, 256, None, None, E16, None) == J.ERR_UNSUPPORTED_DEVICE
 
 
 def test_binding_refuses_cpu_tensors(lib):

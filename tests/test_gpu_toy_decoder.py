@@ -88,3 +88,26 @@ def test_bf16_vs_fp8_mismatch_by_length(model, T):
     print(f"\nT={T}: |dlogp| mean {dlp.mean().item():.3e} max {dlp.max().item():.3e}; "
           f"KL mean {kl.mean().item():.3e} max {kl.max().item():.3e}; top-1 agreement {top1:.4f}")
     assert torch.isfinite(dlp).all() and dlp.max() > 0
+
+
+def test_fused_producers_rollout_equals_training(model):
+    """Rollout with the fused RMSNorm -> FP8 and SwiGLU -> FP8 producers
+    feeding the GEMMs directly gives the same logits, bit for bit, as the
+    training forward that writes the producers' bf16 outputs and lets the
+    linear layers quantise them (and that backpropagates)."""
+    t = tokens(3)
+    with torch.no_grad():
+        rollout = model(t, producers="jetfp8", fused=True)
+        unfused = model(t, producers="jetfp8")
+    train = model(t, producers="jetfp8")
+    assert torch.equal(rollout, unfused)
+    assert torch.equal(rollout, train.detach())
+    loss = torch.nn.functional.cross_entropy(train.float().view(-1, 4096), t.view(-1))
+    loss.backward()
+    assert model.layers[0].n1.grad is not None and torch.isfinite(model.layers[0].n1.grad.float()).all()
+    assert model.layers[1].gate_up.weight.grad.abs().sum() > 0
+    # the producers' forward stays close to the PyTorch reference operators
+    with torch.no_grad():
+        ref = model(t)
+    assert (rollout.float() - ref.float()).abs().max() < 0.25
+    assert jf.jetfp8_poll_device_error() == 0

@@ -24,7 +24,10 @@
 //   warp 1, lane 0 : MMA issuer     -- 4 x tcgen05.mma (K = 32 each) per group
 //                                      into one of two TMEM partial buffers
 //   warp 2         : scale loader   -- cp.async of the group's row scales (128)
-//                                      and column scales into a smem ring
+//                                      and block scales into a smem ring (with
+//                                      per-column scales, both contiguous, the
+//                                      TMA producer fetches them instead, two
+//                                      bulk copies per group)
 //   warps 4..11    : promotion      -- two warpgroups, each 128 rows x BN/2
 //                                      columns; tcgen05.ld the partial, free the
 //                                      buffer, acc += partial * sa * sb (packed
@@ -174,7 +177,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                 ptx::mbar_init(&empty[s], PAIR ? 2 : 1);   // both CTAs' MMA issuers for pairs
             }
             for (int s = 0; s < SCALE_STAGES; ++s) {
-                ptx::mbar_init(&sfull[s], 32);   // every loader lane's copies
+                // per-column scales: the producer's expect-tx arrival; otherwise
+                // every loader lane's copies
+                ptx::mbar_init(&sfull[s], SB_PER_COLUMN ? 1 : 32);
                 ptx::mbar_init(&sempty[s], 8);   // one arrival per promotion warp
             }
             for (uint32_t b = 0; b < NBUF; ++b) {
@@ -206,11 +211,35 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                 int stage = 0;
                 uint32_t phase = 0;
                 uint32_t issued_mask = 0, issued_parity = 0;
+                int ss = 0;
+                uint32_t sphase = 0;
+                bool scale_pending = false;      // a scale copy this thread started may be in flight
                 bool ok = true;
                 for (int tile = work_first; ok && tile < num_work; tile += work_stride) {
                     int tm, tn;
                     coords(tile, tm, tn);
                     for (int g = 0; g < G; ++g) {
+                        if (SB_PER_COLUMN) {
+                            // the group's 128 row scales and the tile's column scales,
+                            // both contiguous: two bulk copies into the next scale slot
+                            if (!ptx::mbar_wait(&sempty[ss], sphase ^ 1u, abort_flag, args.err, ERRBIT_PRODUCER,
+                                                WAIT_TIMEOUT_NS)) {
+                                ok = false;
+                                break;
+                            }
+                            const int ncol = min(BN, args.cols - tn * BN);
+                            float *dst = scl + ss * L::SCALE_FLOATS;
+                            ptx::mbar_arrive_expect_tx(&sfull[ss], (BM + ncol) * 4);
+                            ptx::bulk_load_1d(dst, args.sa + static_cast<int64_t>(g) * args.rows + tm * BM, BM * 4,
+                                              &sfull[ss]);
+                            ptx::bulk_load_1d(dst + BM, args.sb + static_cast<int64_t>(g) * args.sb_stride_g + tn * BN,
+                                              ncol * 4, &sfull[ss]);
+                            scale_pending = true;
+                            if (++ss == SCALE_STAGES) {
+                                ss = 0;
+                                sphase ^= 1u;
+                            }
+                        }
                         if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, args.err, ERRBIT_PRODUCER,
                                             WAIT_TIMEOUT_NS)) {
                             ok = false;
@@ -237,6 +266,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                         if (issued_mask & (1u << s))
                             ptx::mbar_wait(&full[s], (issued_parity >> s) & 1u, nullptr, args.err, ERRBIT_DRAIN,
                                            WAIT_TIMEOUT_NS);
+                    // the scale slots: the most recently filled phase of every slot
+                    if (SB_PER_COLUMN && scale_pending) {
+                        for (int k = 0; k < SCALE_STAGES; ++k) {
+                            const int slot = (ss + SCALE_STAGES - 1 - k) % SCALE_STAGES;
+                            const uint32_t par = slot < ss ? sphase : (sphase ^ 1u);
+                            ptx::mbar_wait(&sfull[slot], par, nullptr, args.err, ERRBIT_DRAIN, WAIT_TIMEOUT_NS);
+                        }
+                    }
                 }
             }
             __syncwarp();
@@ -283,7 +320,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                 ptx::mbar_wait(mma_done, 0, nullptr, args.err, ERRBIT_DRAIN, WAIT_TIMEOUT_NS);
             }
             __syncwarp();
-        } else if (warp == SCALE_WARP) {
+        } else if (warp == SCALE_WARP && !SB_PER_COLUMN) {
             // -------------------------------------------------- scale loader
             int ss = 0;
             uint32_t sphase = 0;

@@ -296,6 +296,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
+    ap.add_argument("--graph", action="store_true",
+                    help="with --case: capture the timed launches into a CUDA graph and time its replay")
     ap.add_argument("--case", default=None,
                     help="time one kernel alone, e.g. fprop:16384x6144x4096 (KIND:MxNxK; KIND in fprop, dgrad, "
                          "wgrad, quant_x, quant_xt, quant_dual, quant_w, rmsnorm_q, swiglu_q) -- a single-kernel line for profiling, "
@@ -428,15 +430,37 @@ def run_case(args):
     for _ in range(args.warmup):
         fn()
     torch.cuda.synchronize()
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
-    evs[0].record()
-    for i in range(args.steps):
-        fn()
-        evs[i + 1].record()
-    torch.cuda.synchronize()
-    times = [evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps)]
+    if args.graph:
+        # the launches captured once into a CUDA graph and replayed: device time
+        # without the host-side cost of each call (what a decode loop replaying
+        # graphs sees)
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side), torch.cuda.graph(graph, stream=side):
+            for _ in range(args.steps):
+                fn()
+        graph.replay()
+        torch.cuda.synchronize()
+        reps = 5
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+        evs[0].record()
+        for i in range(reps):
+            graph.replay()
+            evs[i + 1].record()
+        torch.cuda.synchronize()
+        times = [evs[i].elapsed_time(evs[i + 1]) / args.steps for i in range(reps)]
+    else:
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+        evs[0].record()
+        for i in range(args.steps):
+            fn()
+            evs[i + 1].record()
+        torch.cuda.synchronize()
+        times = [evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps)]
     ms = float(np.median(times))
-    rec = {"case": args.case, "ms_median": round(ms, 5), "ms_min": round(min(times), 5), "launches": args.steps}
+    rec = {"case": args.case, "ms_median": round(ms, 5), "ms_min": round(min(times), 5), "launches": args.steps,
+           "timing": "cuda graph replay" if args.graph else "per-launch events"}
     if kind in ("fprop", "dgrad", "wgrad"):
         rec["tflops"] = round(2.0 * M * N * K / (ms * 1e-3) / 1e12, 1)
     else:

@@ -60,12 +60,15 @@ constexpr int PRODUCER_WARP = 0;
 constexpr int MMA_WARP = 1;
 constexpr int SCALE_WARP = 2;
 constexpr int FIRST_PROMO_WARP = 4;
-constexpr int SCALE_STAGES = 4;
+constexpr int SCALE_STAGES_ALL = 4;      // scale ring slots
+constexpr int MAX_TBUF = 8;              // TMEM partial buffers at most (narrow tiles)
 // setmaxnreg split per tile width: wide tiles keep 128 accumulator registers
 // per promotion thread, 128-wide tiles 64 (which leaves the control warps room).
 template <int BN> struct RegSplit;
 template <> struct RegSplit<256> { static constexpr uint32_t CTRL = 40, PROMO = 232; };
 template <> struct RegSplit<128> { static constexpr uint32_t CTRL = 88, PROMO = 200; };
+template <> struct RegSplit<64> { static constexpr uint32_t CTRL = 88, PROMO = 200; };
+template <> struct RegSplit<32> { static constexpr uint32_t CTRL = 88, PROMO = 200; };
 static_assert(128 * RegSplit<256>::CTRL + 256 * RegSplit<256>::PROMO <= NUM_THREADS * 168, "register split");
 static_assert(128 * RegSplit<128>::CTRL + 256 * RegSplit<128>::PROMO <= NUM_THREADS * 168, "register split");
 constexpr int GROUP_M = 16;              // tile rasterisation: m-tiles per band
@@ -92,14 +95,16 @@ struct Smem {
     // scale ring: per slot 128 row scales then BN column scales (fp32)
     static constexpr uint32_t SCALE_FLOATS = BM + BN;
     static constexpr uint32_t SCALE_OFF = TILES;
+    static constexpr int SCALE_STAGES = SCALE_STAGES_ALL;
     static constexpr uint32_t SCALE_BYTES = SCALE_STAGES * SCALE_FLOATS * 4;
     // epilogue staging: per promotion warp two 32-row x 16-column bf16 chunks
     static constexpr uint32_t OUT_OFF = SCALE_OFF + SCALE_BYTES;
     static constexpr uint32_t OUT_CHUNK_BYTES = 32 * 16 * 2;
     static constexpr uint32_t OUT_BYTES = 8 * 2 * OUT_CHUNK_BYTES;
     static constexpr uint32_t BAR_OFF = OUT_OFF + OUT_BYTES;
-    // full[S], empty[S], sfull[SS], sempty[SS], tfull[4], tempty[4], mma_done, tmem holder, abort flag
-    static constexpr uint32_t CTRL_BYTES = (2 * STAGES + 2 * SCALE_STAGES + 9) * 8 + 16;
+    // full[S], empty[S], sfull[SS], sempty[SS], tfull[MAX_TBUF], tempty[MAX_TBUF], mma_done,
+    // tmem holder, abort flag
+    static constexpr uint32_t CTRL_BYTES = (2 * STAGES + 2 * SCALE_STAGES + 2 * MAX_TBUF + 1) * 8 + 16;
     static constexpr uint32_t TOTAL = 1024 /* alignment slack */ + BAR_OFF + CTRL_BYTES;
 };
 
@@ -133,10 +138,18 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
             const __grid_constant__ CUtensorMap tmap_d, const KernelArgs args)
 {
     using L = Smem<BN, STAGES>;
-    constexpr int COLS_PER_WG = BN / 2;          // columns per promotion warpgroup
+    constexpr int SCALE_STAGES = L::SCALE_STAGES;
+    // Tiles 128 or 256 wide: two promotion warpgroups, one per column half.
+    // Narrow tiles (decode-sized problems): the first warpgroup alone.
+    constexpr int NWG = BN >= 128 ? 2 : 1;
+    constexpr int COLS_PER_WG = BN / NWG;        // columns per promotion warpgroup
     constexpr int CHUNKS = COLS_PER_WG / 32;     // tcgen05.ld x32 per group
-    static_assert(CHUNKS % 2 == 0, "loads are issued in pairs");
-    constexpr uint32_t NBUF = PAIR ? 4 : 2;      // TMEM partial buffers
+    constexpr int LPW = CHUNKS >= 2 ? 2 : 1;     // loads in flight per wait
+    static_assert(CHUNKS % LPW == 0, "loads are issued in pairs");
+    // TMEM partial buffers: two 256- or 128-wide ones, four for CTA pairs,
+    // eight for narrow (decode) tiles, so that the MMAs can run up to eight
+    // groups ahead of the read-back instead of waiting on every hand-off.
+    constexpr uint32_t NBUF = PAIR ? 4 : (BN >= 128 ? 2 : MAX_TBUF);
     constexpr uint32_t TMEM_COLS = NBUF * BN;
     static_assert(TMEM_COLS <= 512, "TMEM holds 512 columns");
     constexpr uint32_t IDESC = ptx::idesc_e4m3_f32(BM, BN);
@@ -151,8 +164,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     uint64_t *sfull = empty + STAGES;
     uint64_t *sempty = sfull + SCALE_STAGES;
     uint64_t *tfull = sempty + SCALE_STAGES;
-    uint64_t *tempty = tfull + 4;
-    uint64_t *mma_done = tempty + 4;
+    uint64_t *tempty = tfull + MAX_TBUF;
+    uint64_t *mma_done = tempty + MAX_TBUF;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(mma_done + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
 
@@ -180,11 +193,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                 // per-column scales: the producer's expect-tx arrival; otherwise
                 // every loader lane's copies
                 ptx::mbar_init(&sfull[s], SB_PER_COLUMN ? 1 : 32);
-                ptx::mbar_init(&sempty[s], 8);   // one arrival per promotion warp
+                ptx::mbar_init(&sempty[s], 4 * NWG);   // one arrival per promotion warp
             }
             for (uint32_t b = 0; b < NBUF; ++b) {
                 ptx::mbar_init(&tfull[b], 1);
-                ptx::mbar_init(&tempty[b], 8);   // one arrival per promotion warp
+                ptx::mbar_init(&tempty[b], 4 * NWG);   // one arrival per promotion warp
             }
             ptx::mbar_init(mma_done, 1);
             *abort_flag = 0;
@@ -352,7 +365,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                             const bool in = col < args.cols;
                             ptx::cp_async_16z(dst + BM + c, in ? sb_g + col : args.sb, in ? 16u : 0u);
                         }
-                    } else if (lane < BN / 128) {
+                    } else if (lane < (BN >= 128 ? BN / 128 : 1)) {
                         const int col = tn * BN + lane * 128;
                         const bool in = col < args.cols;
                         ptx::cp_async_4(dst + BM + lane,
@@ -372,6 +385,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         ptx::setmaxnreg_inc<RegSplit<BN>::PROMO>();
         // ------------------------------------------------------ promotion
         const int wg = (warp - FIRST_PROMO_WARP) >> 2;   // 0 or 1: column half of the tile
+        // (with narrow tiles the second warpgroup has no columns and skips the loop)
         const int quarter = warp & 3;                    // TMEM lanes 32*quarter .. +31
         const int row_in_tile = quarter * 32 + lane;
         uint8_t *out_stage = smem + L::OUT_OFF + (warp - FIRST_PROMO_WARP) * 2 * L::OUT_CHUNK_BYTES;
@@ -379,7 +393,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         int ss = 0;
         uint32_t sphase = 0;
         bool ok = true;
-        for (int tile = work_first; ok && tile < num_work; tile += work_stride) {
+        for (int tile = work_first; ok && wg < NWG && tile < num_work; tile += work_stride) {
             int tm, tn;
             coords(tile, tm, tn);
             const int col0 = tn * BN + wg * COLS_PER_WG;
@@ -420,50 +434,51 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                 ptx::tc_fence_after();
                 const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + buf * BN +
                                        wg * COLS_PER_WG;
-                // Two 32-column loads in flight per wait (64 columns), so each
-                // group pays the TMEM load latency only COLS_PER_WG / 64 times.
+                // acc += partial * scale for 32 columns starting at column c0
+                // of this warpgroup's range
+                auto apply32 = [&](const uint32_t(&p)[32], const int c0) {
+                    if (SB_PER_COLUMN) {
+                        // acc += p * (sa * sb[col]): the products two at a time,
+                        // the accumulation in plain fp32 FMAs
+                        const uint64_t sa2 = ptx::pack_f32x2(sa, sa);
+                        const uint64_t *sbv = reinterpret_cast<const uint64_t *>(sbcol + c0);
+                        float *a = acc1 + c0;
 #pragma unroll
-                for (int h = 0; h < CHUNKS / 2; ++h) {
+                        for (int i = 0; i < 16; ++i) {
+                            const uint64_t w = ptx::mul_f32x2(sa2, sbv[i]);
+                            a[2 * i] = fmaf(__uint_as_float(p[2 * i]), ptx::lo_f32(w), a[2 * i]);
+                            a[2 * i + 1] = fmaf(__uint_as_float(p[2 * i + 1]), ptx::hi_f32(w), a[2 * i + 1]);
+                        }
+                    } else {
+                        const uint64_t w2 = ptx::pack_f32x2(w_blk, w_blk);
+                        uint64_t *a0 = acc2 + c0 / 2;
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            ptx::fma_f32x2(a0[i], ptx::pack_f32x2(p[2 * i], p[2 * i + 1]), w2);
+                    }
+                };
+                // Two 32-column loads in flight per wait (64 columns) where the
+                // warpgroup's range allows, so each group pays the TMEM load
+                // latency only COLS_PER_WG / 64 times.
+#pragma unroll
+                for (int h = 0; h < CHUNKS / LPW; ++h) {
                     uint32_t p0[32], p1[32];
-                    ptx::tmem_ld_32x32b_x32(taddr + h * 64, p0);
-                    ptx::tmem_ld_32x32b_x32(taddr + h * 64 + 32, p1);
+                    ptx::tmem_ld_32x32b_x32(taddr + h * 32 * LPW, p0);
+                    if (LPW == 2)
+                        ptx::tmem_ld_32x32b_x32(taddr + h * 64 + 32, p1);
                     ptx::tmem_ld_wait(p0);
-                    ptx::tmem_ld_wait(p1);
-                    if (h + 1 == CHUNKS / 2) {
+                    if (LPW == 2)
+                        ptx::tmem_ld_wait(p1);
+                    if (h + 1 == CHUNKS / LPW) {
                         // the whole partial is in registers: hand the buffer back
                         ptx::tc_fence_before();
                         __syncwarp();
                         if (lane == 0)
                             ptx::mbar_arrive(&tempty[buf]);
                     }
-                    if (SB_PER_COLUMN) {
-                        // acc += p * (sa * sb[col]): the products two at a time,
-                        // the accumulation in plain fp32 FMAs
-                        const uint64_t sa2 = ptx::pack_f32x2(sa, sa);
-                        const uint64_t *sbv = reinterpret_cast<const uint64_t *>(sbcol + h * 64);
-                        float *a = acc1 + h * 64;
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const uint64_t w = ptx::mul_f32x2(sa2, sbv[i]);
-                            a[2 * i] = fmaf(__uint_as_float(p0[2 * i]), ptx::lo_f32(w), a[2 * i]);
-                            a[2 * i + 1] = fmaf(__uint_as_float(p0[2 * i + 1]), ptx::hi_f32(w), a[2 * i + 1]);
-                        }
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const uint64_t w = ptx::mul_f32x2(sa2, sbv[16 + i]);
-                            a[32 + 2 * i] = fmaf(__uint_as_float(p1[2 * i]), ptx::lo_f32(w), a[32 + 2 * i]);
-                            a[32 + 2 * i + 1] = fmaf(__uint_as_float(p1[2 * i + 1]), ptx::hi_f32(w), a[32 + 2 * i + 1]);
-                        }
-                    } else {
-                        const uint64_t w2 = ptx::pack_f32x2(w_blk, w_blk);
-                        uint64_t *a0 = acc2 + h * 32;
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            ptx::fma_f32x2(a0[i], ptx::pack_f32x2(p0[2 * i], p0[2 * i + 1]), w2);
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            ptx::fma_f32x2(a0[16 + i], ptx::pack_f32x2(p1[2 * i], p1[2 * i + 1]), w2);
-                    }
+                    apply32(p0, h * 32 * LPW);
+                    if (LPW == 2)
+                        apply32(p1, h * 64 + 32);
                 }
                 if (SB_PER_COLUMN) {
                     __syncwarp();
@@ -533,6 +548,7 @@ cudaError_t launch_variant(const GemmProblem &p, const DeviceInfo &dev, const CU
                            const CUtensorMap &td, cudaStream_t stream)
 {
     using L = Smem<BN, STAGES>;
+    static_assert(L::TOTAL <= 227 * 1024, "shared memory per CTA");
     auto kern = gemm_kernel<BN, STAGES, SB_PER_COLUMN, PAIR>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(L::TOTAL));
     if (e != cudaSuccess)
@@ -612,12 +628,25 @@ CUresult encode_output(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap *ma
 cudaError_t launch_gemm(const GemmProblem &p, const DeviceInfo &dev, PFN_cuTensorMapEncodeTiled_v12000 encode,
                         cudaStream_t stream)
 {
-    // 128 x 256 tiles, unless they would leave most SMs idle (small problems):
-    // then 128 x 128 tiles.
-    const int64_t tiles256 = ((p.rows + BM - 1) / BM) * ((p.cols + 255) / 256);
-    const bool wide = tiles256 >= dev.sm_count;
+    // Tile width: the fewest waves of tiles over the SMs, and among widths
+    // with that many waves the narrowest (more CTAs streaming B).  A tile's
+    // time is set mostly by its number of K groups, not its width, so extra
+    // waves cost more than idle SMs (measured on the 8B-class decode shapes:
+    // this rule picks the fastest width on every one).  Training-sized
+    // problems get 128 x 256 tiles.  The width never changes how an output
+    // element is reduced.
+    const int64_t tm_count = (p.rows + BM - 1) / BM;
     const bool pair = false;   // CTA pairs of 128 x 128 tiles: measured slower than wide tiles so far
-    const int bn = (wide && !pair) ? 256 : 128;
+    int bn = 256;
+    int64_t best_waves = -1;
+    for (int w : {256, 128, 64, 32}) {
+        const int64_t tiles = tm_count * ((p.cols + w - 1) / w);
+        const int64_t waves = (tiles + dev.sm_count - 1) / dev.sm_count;
+        if (best_waves < 0 || waves <= best_waves) {   // ties: the narrower width (later in the list)
+            best_waves = waves;
+            bn = w;
+        }
+    }
     CUtensorMap ta, tb, td;
     if (encode_operand(encode, &ta, p.a, p.rows, p.kdim, pair ? BM / 2 : BM) != CUDA_SUCCESS ||
         encode_operand(encode, &tb, p.b, p.cols, p.kdim, bn) != CUDA_SUCCESS ||
@@ -627,11 +656,20 @@ cudaError_t launch_gemm(const GemmProblem &p, const DeviceInfo &dev, PFN_cuTenso
     if (pair)
         return per_col ? launch_variant<128, 6, true, true>(p, dev, ta, tb, td, stream)
                        : launch_variant<128, 6, false, true>(p, dev, ta, tb, td, stream);
-    if (wide)
+    switch (bn) {
+    case 256:
         return per_col ? launch_variant<256, 4, true, false>(p, dev, ta, tb, td, stream)
                        : launch_variant<256, 4, false, false>(p, dev, ta, tb, td, stream);
-    return per_col ? launch_variant<128, 6, true, false>(p, dev, ta, tb, td, stream)
-                   : launch_variant<128, 6, false, false>(p, dev, ta, tb, td, stream);
+    case 128:
+        return per_col ? launch_variant<128, 6, true, false>(p, dev, ta, tb, td, stream)
+                       : launch_variant<128, 6, false, false>(p, dev, ta, tb, td, stream);
+    case 64:
+        return per_col ? launch_variant<64, 8, true, false>(p, dev, ta, tb, td, stream)
+                       : launch_variant<64, 8, false, false>(p, dev, ta, tb, td, stream);
+    default:
+        return per_col ? launch_variant<32, 9, true, false>(p, dev, ta, tb, td, stream)
+                       : launch_variant<32, 9, false, false>(p, dev, ta, tb, td, stream);
+    }
 }
 
 // ---------------------------------------------------------------------------

@@ -38,6 +38,17 @@ class QuantizedWeight:
         return self.q, self.s, self.qt
 
 
+_SIDE_STREAMS = {}
+
+
+def _side_stream(device) -> torch.cuda.Stream:
+    """One extra stream per device for the backward's Wgrad."""
+    key = torch.device(device).index
+    if key not in _SIDE_STREAMS:
+        _SIDE_STREAMS[key] = torch.cuda.Stream(device=device)
+    return _SIDE_STREAMS[key]
+
+
 class FP8LinearFunction(torch.autograd.Function):
     """y = x W^T with FP8 Fprop; FP8 Dgrad and Wgrad in backward."""
 
@@ -66,6 +77,20 @@ class FP8LinearFunction(torch.autograd.Function):
             qdy, sdy = _j.quantize_act(dy)
         elif ctx.needs_input_grad[1]:
             qdyt, sdyt = _j.quantize_act_transposed(dy)
+        if ctx.needs_input_grad[0] and ctx.needs_input_grad[1]:
+            # Dgrad and Wgrad are independent: Wgrad runs on a side stream so
+            # that each GEMM's last partial wave of tiles is filled by the other
+            main = torch.cuda.current_stream(dy.device)
+            side = _side_stream(dy.device)
+            side.wait_stream(main)
+            with torch.cuda.stream(side):
+                dw = _j.gemm_wgrad(qdyt, sdyt, qxt, sxt)
+            for t in (qdyt, sdyt, qxt, sxt):
+                t.record_stream(side)
+            dx = _j.gemm_dgrad(qdy, sdy, qt, s)
+            main.wait_stream(side)
+            dw.record_stream(main)
+            return dx, dw, None
         if ctx.needs_input_grad[0]:
             dx = _j.gemm_dgrad(qdy, sdy, qt, s)
         if ctx.needs_input_grad[1]:

@@ -62,15 +62,17 @@ __device__ __forceinline__ float exp_f32(float x)
     return __fmul_rn(__fmul_rn(p, pow2_normal(n1)), pow2_normal(ni - n1));
 }
 
-__device__ __forceinline__ float round_bf16(float v)
+// Round eight fp32 values to bf16 (nearest even), two per conversion: the
+// bf16 words (value 2k in the low half of word k) and their fp32 values.
+__device__ __forceinline__ void round_bf16x8(const float (&v)[8], uint32_t (&w)[4], float (&r)[8])
 {
-    return __bfloat162float(__float2bfloat16_rn(v));
-}
-
-__device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi)
-{
-    // both values are already bf16-exact: the conversion only moves bits
-    return (__float_as_uint(lo) >> 16) | (__float_as_uint(hi) & 0xFFFF0000u);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * k], v[2 * k + 1]);
+        w[k] = *reinterpret_cast<const uint32_t *>(&h);
+        r[2 * k] = bf16_lo(w[k]);
+        r[2 * k + 1] = bf16_hi(w[k]);
+    }
 }
 
 // The eight bf16-exact values v of this lane belong to the 1x128 group of
@@ -141,15 +143,16 @@ rmsnorm_quantize_kernel(const uint4 *__restrict__ x, const uint4 *__restrict__ g
 #pragma unroll 4
     for (int j = 0; j < nj; ++j) {
         const int64_t c = 32 * j + lane;
-        float f[8], g[8], v[8];
+        float f[8], g[8], u[8], v[8];
         unpack8(__ldg(xr + c), f);
         unpack8(__ldg(gamma + c), g);
 #pragma unroll
         for (int e = 0; e < 8; ++e)
-            v[e] = round_bf16(__fmul_rn(__fmul_rn(f[e], rstd), g[e]));
+            u[e] = __fmul_rn(__fmul_rn(f[e], rstd), g[e]);
+        uint32_t w[4];
+        round_bf16x8(u, w, v);
         if (y)
-            y[row * H8 + c] = make_uint4(pack2_bf16(v[0], v[1]), pack2_bf16(v[2], v[3]), pack2_bf16(v[4], v[5]),
-                                         pack2_bf16(v[6], v[7]));
+            y[row * H8 + c] = make_uint4(w[0], w[1], w[2], w[3]);
         if (q)
             quantize8_halfwarp(v, q + row * H + 8 * c, s + (c >> 4) * M + row, lane);
     }
@@ -173,18 +176,19 @@ swiglu_quantize_kernel(const uint4 *__restrict__ gu, int64_t M, int64_t I, uint8
          it += static_cast<int64_t>(gridDim.x) * PR_WARPS) {
         const int64_t row = it / chunks;
         const int64_t c = (it - row * chunks) * 32 + lane;   // output uint4 index within the row
-        float g[8], u[8], v[8];
+        float g[8], u[8], t[8], v[8];
         unpack8(__ldg(gu + row * in_row + c), g);
         unpack8(__ldg(gu + row * in_row + out_row + c), u);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             // 1 / (1 + e^-g): the correctly rounded reciprocal is the IEEE quotient
             const float sig = __frcp_rn(__fadd_rn(1.0f, exp_f32(-g[e])));
-            v[e] = round_bf16(__fmul_rn(__fmul_rn(g[e], sig), u[e]));
+            t[e] = __fmul_rn(__fmul_rn(g[e], sig), u[e]);
         }
+        uint32_t w[4];
+        round_bf16x8(t, w, v);
         if (y)
-            y[row * out_row + c] = make_uint4(pack2_bf16(v[0], v[1]), pack2_bf16(v[2], v[3]),
-                                              pack2_bf16(v[4], v[5]), pack2_bf16(v[6], v[7]));
+            y[row * out_row + c] = make_uint4(w[0], w[1], w[2], w[3]);
         if (q)
             quantize8_halfwarp(v, q + row * I + 8 * c, s + (c >> 4) * M + row, lane);
     }

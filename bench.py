@@ -157,27 +157,35 @@ class Step:
             ("wgrad", lambda: jf.jetfp8_gemm_wgrad(d["qdyt"], d["sdyt"], d["qxt"], d["sxt"], d["dw"])),
         )
 
-    def run(self, events=None, side=None):
-        """Enqueue one step on the current stream.  With `side` (a second
-        stream), each projection's dY quantisation and Wgrad run there: dY's
-        quantisation overlaps the W and X quantisations, and Wgrad (after X's
-        transposed codes exist) overlaps Fprop and Dgrad (after dY's codes
-        exist), so one GEMM's last partial wave of tiles is filled by the
-        other's; the current stream waits for the side stream at the end.
-        With `events`, every launch is bracketed by (start, end) events on the
-        stream it runs on."""
+    def run(self, events=None, side=None, quant=None):
+        """Enqueue one step on the current stream.
+
+        With `side` (a second stream), each projection's dY quantisation and
+        Wgrad run there: dY's quantisation overlaps the W and X quantisations,
+        and Wgrad (after X's transposed codes exist) overlaps Fprop and Dgrad
+        (after dY's codes exist), so one GEMM's last partial wave of tiles is
+        filled by the other's.  With `quant` as well (a third stream), all
+        quantisations run there in projection order, ahead of the GEMMs that
+        need them, so they can also fill GEMM tails.  The current stream waits
+        for the others at the end.  With `events`, every launch is bracketed
+        by (start, end) events on the stream it runs on."""
         main = torch.cuda.current_stream()
-        if side is not None:
-            side.wait_stream(main)
+        for st in (side, quant):
+            if st is not None:
+                st.wait_stream(main)
         for name, d in self.p.items():
-            x_ready = dy_ready = None
+            x_ready = dy_ready = w_ready = None
             for kind, fn in self.launches(d):
-                on_side = side is not None and kind in ("quant_dy_dual", "wgrad")
-                s = side if on_side else main
-                if side is not None and kind == "wgrad":
-                    s.wait_event(x_ready)
-                if side is not None and kind == "dgrad":
-                    s.wait_event(dy_ready)
+                if quant is not None and kind.startswith("quant"):
+                    s = quant
+                elif side is not None and kind in ("quant_dy_dual", "wgrad"):
+                    s = side
+                else:
+                    s = main
+                if kind in ("fprop", "dgrad", "wgrad"):
+                    for ev in (w_ready, x_ready, dy_ready):
+                        if ev is not None:
+                            s.wait_event(ev)
                 with torch.cuda.stream(s):
                     ev0 = ev1 = None
                     if events is not None:
@@ -188,14 +196,21 @@ class Step:
                         ev1 = torch.cuda.Event(enable_timing=True)
                         ev1.record(s)
                         events.append((name, kind, ev0, ev1))
-                if side is not None and kind == "quant_x_dual":
+                if s is not main and kind.startswith("quant"):
+                    ev = torch.cuda.Event()
+                    ev.record(s)
+                    if kind == "quant_w":
+                        w_ready = ev
+                    elif kind == "quant_x_dual":
+                        x_ready = ev
+                    else:
+                        dy_ready = ev
+                elif kind == "quant_x_dual" and side is not None:
                     x_ready = torch.cuda.Event()
                     x_ready.record(main)
-                if side is not None and kind == "quant_dy_dual":
-                    dy_ready = torch.cuda.Event()
-                    dy_ready.record(side)
-        if side is not None:
-            main.wait_stream(side)
+        for st in (side, quant):
+            if st is not None:
+                main.wait_stream(st)
 
 
 def time_ours(args, rank, world, device):
@@ -203,9 +218,10 @@ def time_ours(args, rank, world, device):
     serial pass afterwards gives each kernel's own duration (for the
     per-kernel breakdown and the roofline), free of overlap."""
     step = Step(device, seed=1000 + rank)
-    side = torch.cuda.Stream(device=device)
+    side = torch.cuda.Stream(device=device) if args.streams >= 2 else None
+    quant = torch.cuda.Stream(device=device) if args.streams >= 3 else None
     for _ in range(args.warmup):
-        step.run(side=side)
+        step.run(side=side, quant=quant)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
@@ -216,7 +232,7 @@ def time_ours(args, rank, world, device):
     with ClockSampler(torch.cuda.current_device()) as clk:
         start.record()
         for _ in range(args.steps):
-            step.run(side=side)
+            step.run(side=side, quant=quant)
         end.record()
         torch.cuda.synchronize()
     if world > 1:
@@ -363,6 +379,9 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
+    ap.add_argument("--streams", type=int, default=2, choices=(1, 2, 3),
+                    help="streams the timed step runs on: 1 serial; 2 Wgrad and dY's quantisation beside the "
+                         "rest; 3 all quantisations on a third stream as well")
     ap.add_argument("--graph", action="store_true",
                     help="with --case: capture the timed launches into a CUDA graph and time its replay")
     ap.add_argument("--case", default=None,

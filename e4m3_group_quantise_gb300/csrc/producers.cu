@@ -75,31 +75,6 @@ __device__ __forceinline__ void round_bf16x8(const float (&v)[8], uint32_t (&w)[
     }
 }
 
-// The eight bf16-exact values v of this lane belong to the 1x128 group of
-// its half-warp: group amax, scale, codes (written at q8) and, from the
-// half-warp's first lane, the scale (written at *scale).
-__device__ __forceinline__ void quantize8_halfwarp(const float (&v)[8], uint8_t *q8, float *scale, int lane)
-{
-    float amax = 0.0f;
-#pragma unroll
-    for (int e = 0; e < 8; ++e)
-        amax = fmaxf(amax, fabsf(v[e]));
-#pragma unroll
-    for (int d = 8; d >= 1; d >>= 1)
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
-    const GroupScale gs = group_scale(amax);
-    uint32_t w[2];
-    const uint32_t redo = encode_words<2>(v, gs, w);
-    // rare: a word whose bracket disagreed takes the exact quotient
-    if (redo & 1u)
-        w[0] = encode4_exact(v[0], v[1], v[2], v[3], gs.s);
-    if (redo & 2u)
-        w[1] = encode4_exact(v[4], v[5], v[6], v[7], gs.s);
-    *reinterpret_cast<uint2 *>(q8) = make_uint2(w[0], w[1]);
-    if ((lane & 15) == 0)
-        *scale = gs.s;
-}
-
 // ---------------------------------------------------------------------------
 // RMSNorm: one warp per row.  Pass 1 sums the squares: lane l adds, in order,
 // the squares of its chunks' values (chunk 32 j + l, j = 0, 1, ...), then the
@@ -112,9 +87,11 @@ __device__ __forceinline__ float sum_squares8(float acc, const uint4 &c)
 {
     float f[8];
     unpack8(c, f);
+    // x^2 of a bf16 value is exact in fp32, so the fused multiply-add rounds
+    // exactly as the separate multiply and add would
 #pragma unroll
     for (int e = 0; e < 8; ++e)
-        acc = __fadd_rn(acc, __fmul_rn(f[e], f[e]));
+        acc = fmaf(f[e], f[e], acc);
     return acc;
 }
 

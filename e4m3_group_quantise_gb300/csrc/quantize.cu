@@ -274,157 +274,157 @@ quantize_weight_kernel(const uint4 *__restrict__ w, int64_t N, int64_t K, uint2 
 // ---------------------------------------------------------------------------
 // Dual output: one read of X [M][K] yields both the 1x128 row-group codes and
 // scales (as quantize_act_kernel) and the 128x1 column-group codes and scales
-// written transposed (as quantize_act_t_kernel).  Persistent CTAs walk 128 x
-// 128 tiles; each tile is copied (cp.async) into one of two shared-memory
-// buffers while the previous tile is quantised, 16-byte chunks XOR-swizzled by
-// (row & 15) so that both read patterns below are bank-conflict free.
-//   rows:    thread (r = t % 128, half h = t / 128) reads 64 values of row r;
-//            the two halves combine their amax through shared memory; each
-//            thread writes 64 contiguous codes; h == 0 writes the row's scale.
-//   columns: warp w covers rows 32*(w>>1) .. +31 and column pairs
-//            32*(w&1) + lane; the four row quarters combine their amax through
-//            shared memory; each thread writes 32 contiguous codes per column.
-// The arithmetic of every group is exactly that of the single-output kernels.
+// written transposed (as quantize_act_t_kernel).  One CTA (8 warps) per 128 x
+// 128 tile:
+//   rows:    warp w loads rows 16w .. 16w+15 straight from global memory,
+//            eight rows per step, four lanes per row holding 32 values each
+//            (16-byte chunks sub, sub + 4, sub + 8, sub + 12), and encodes them
+//            as it goes: one scale per 32 values per lane, amax in two
+//            shuffles, codes in 32-byte runs.  The raw values also go to a
+//            shared tile, 16-byte chunks XOR-swizzled by (row & 15).
+//   columns: after one block barrier, warp w takes 8-column chunk w (then
+//            w + 8) and reads it with four transposing matrix loads
+//            (ldmatrix .trans, 32 rows each, conflict-free thanks to the
+//            swizzle): lane 4c + q then holds column c, rows 8j + 2q and
+//            8j + 2q + 1 for j = 0..15, so a 128x1 group is four lanes of one
+//            warp (amax: two shuffles).  The interleaved codes are put back in
+//            row order through a small per-warp staging buffer and leave as
+//            two 16-byte stores per lane.
 // ---------------------------------------------------------------------------
 constexpr int QD_TILE = 128;
 constexpr int QD_THREADS = 256;
-constexpr int QD_CTAS_PER_SM = 3;
+constexpr int QD_STAGE_PITCH = 140;          // bytes per staged column (35 words: writes and reads bank-conflict free)
 
 struct DualSmem {
-    uint4 tile[2][QD_TILE][QD_TILE / 8];
-    float ramax[2][QD_TILE];
-    float2 camax[4][QD_TILE / 2];
+    uint4 tile[QD_TILE][QD_TILE / 8];                          // 32 KB
+    uint8_t stage[QD_THREADS / 32][8][QD_STAGE_PITCH];        // codes of 8 columns per warp
 };
 
-__device__ __forceinline__ void dual_issue_tile(DualSmem &sm, int buf, const uint4 *x, int64_t K8, int64_t m0,
-                                                int64_t k0, int t)
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], const void *row_addr)
 {
-#pragma unroll
-    for (int p = 0; p < 8; ++p) {
-        const int idx = p * QD_THREADS + t;          // 16 chunks per row
-        const int r = idx >> 4, c = idx & 15;
-        ptx::cp_async_16(&sm.tile[buf][r][c ^ (r & 15)], x + (m0 + r) * K8 + (k0 >> 3) + c);
-    }
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(ptx::smem_u32(row_addr))
+                 : "memory");
 }
 
-__global__ void __launch_bounds__(QD_THREADS, QD_CTAS_PER_SM)
+__global__ void __launch_bounds__(QD_THREADS)
 quantize_act_dual_kernel(const uint4 *__restrict__ x, int64_t M, int64_t K, uint8_t *__restrict__ q,
                          float *__restrict__ s, uint8_t *__restrict__ qt, float *__restrict__ st)
 {
     extern __shared__ __align__(16) uint8_t dual_smem_raw[];
     DualSmem &sm = *reinterpret_cast<DualSmem *>(dual_smem_raw);
-    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t K8 = K >> 3;
     const int64_t tiles_k = K / QD_TILE;
-    const int64_t n_tiles = (M / QD_TILE) * tiles_k;
+    const int64_t m0 = (static_cast<int64_t>(blockIdx.x) / tiles_k) * QD_TILE;
+    const int64_t k0 = (static_cast<int64_t>(blockIdx.x) % tiles_k) * QD_TILE;
 
-    int64_t tile = blockIdx.x;
-    if (tile < n_tiles)
-        dual_issue_tile(sm, 0, x, K8, (tile / tiles_k) * QD_TILE, (tile % tiles_k) * QD_TILE, t);
-    ptx::cp_async_commit();
-    for (int it = 0; tile < n_tiles; ++it, tile += gridDim.x) {
-        const int buf = it & 1;
-        const int64_t m0 = (tile / tiles_k) * QD_TILE, k0 = (tile % tiles_k) * QD_TILE;
-        const int64_t next = tile + gridDim.x;
-        if (next < n_tiles)
-            dual_issue_tile(sm, buf ^ 1, x, K8, (next / tiles_k) * QD_TILE, (next % tiles_k) * QD_TILE, t);
-        ptx::cp_async_commit();
-        ptx::cp_async_wait<1>();                      // this tile's copies have landed
-        __syncthreads();
-        const uint4 (*tl)[QD_TILE / 8] = sm.tile[buf];
-
-        // ---- 1x128 groups along rows -------------------------------------
-        {
-            const int r = t & 127, h = t >> 7;
-            float f[64];
+    // ---- rows: 16 per warp, 8 per step; four lanes per row, 32 values each
+    //      (16-byte chunks sub, sub+4, sub+8, sub+12 of the row's 256 bytes)
+    {
+        const int rr = lane >> 2, sub = lane & 3;
+#pragma unroll
+        for (int step = 0; step < 2; ++step) {
+            const int r = 16 * warp + 8 * step + rr;
+            const uint4 *src = x + (m0 + r) * K8 + (k0 >> 3);
+            uint4 v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                v[j] = __ldg(src + sub + 4 * j);
+            float f[32];
             float amax = 0.0f;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
+            for (int j = 0; j < 4; ++j) {
+                const int c = sub + 4 * j;
+                sm.tile[r][c ^ (r & 15)] = v[j];
                 float u[8];
-                unpack8(tl[r][(8 * h + j) ^ (r & 15)], u);
+                unpack8(v[j], u);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     f[8 * j + e] = u[e];
                     amax = fmaxf(amax, fabsf(u[e]));
                 }
             }
-            sm.ramax[h][r] = amax;
-            __syncthreads();
-            amax = fmaxf(sm.ramax[0][r], sm.ramax[1][r]);
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
             const GroupScale gs = group_scale(amax);
-            uint32_t w[16];
-            uint32_t redo = encode_words<16>(f, gs, w);
-            uint8_t *row_out = q + (m0 + r) * K + k0 + 64 * h;
-            uint4 *dst = reinterpret_cast<uint4 *>(row_out);
+            uint32_t w[8];
+            const uint32_t redo = encode_words<8>(f, gs, w);
+            if (redo != 0u) {        // rare: the exact quotient for flagged words
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                __stcs(dst + j, make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]));
-            if (h == 0)
+                for (int k = 0; k < 8; ++k)
+                    if (redo & (1u << k))
+                        w[k] = encode4_exact(f[4 * k], f[4 * k + 1], f[4 * k + 2], f[4 * k + 3], gs.s);
+            }
+            uint8_t *row_q = q + (m0 + r) * K + k0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)      // the row's four lanes write 32 contiguous bytes per j
+                *reinterpret_cast<uint2 *>(row_q + 8 * (sub + 4 * j)) = make_uint2(w[2 * j], w[2 * j + 1]);
+            if (sub == 0)
                 s[(k0 >> 7) * M + m0 + r] = gs.s;
-            // rare: words whose bracket disagreed get the exact quotient
-            while (redo != 0u) {
-                const int k = __ffs(redo) - 1;
-                redo &= redo - 1u;
-                const uint2 in = reinterpret_cast<const uint2 *>(&tl[r][(8 * h + (k >> 1)) ^ (r & 15)])[k & 1];
-                *reinterpret_cast<uint32_t *>(row_out + 4 * k) = encode4_exact(in, gs.s);
-            }
         }
-
-        // ---- 128x1 groups along columns, written transposed ---------------
-        {
-            const int qd = warp >> 1;                   // row quarter
-            const int p = 32 * (warp & 1) + lane;       // column pair
-            float f0[32], f1[32];
-            float a0 = 0.0f, a1 = 0.0f;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int r = 32 * qd + i;
-                const uint32_t wv = reinterpret_cast<const uint32_t *>(&tl[r][0])[(((p >> 2) ^ (r & 15)) << 2) + (p & 3)];
-                f0[i] = bf16_lo(wv);
-                f1[i] = bf16_hi(wv);
-                a0 = fmaxf(a0, fabsf(f0[i]));
-                a1 = fmaxf(a1, fabsf(f1[i]));
-            }
-            sm.camax[qd][p] = make_float2(a0, a1);
-            __syncthreads();
-#pragma unroll
-            for (int kq = 0; kq < 4; ++kq) {
-                const float2 o = sm.camax[kq][p];
-                a0 = fmaxf(a0, o.x);
-                a1 = fmaxf(a1, o.y);
-            }
-            const GroupScale g0 = group_scale(a0), g1 = group_scale(a1);
-            uint32_t w0[8], w1[8];
-            uint32_t redo = encode_words<8>(f0, g0, w0) | (encode_words<8>(f1, g1, w1) << 8);
-            const int64_t col = k0 + 2 * p;
-            uint4 *d0 = reinterpret_cast<uint4 *>(qt + col * M + m0 + 32 * qd);
-            uint4 *d1 = reinterpret_cast<uint4 *>(qt + (col + 1) * M + m0 + 32 * qd);
-            __stcs(d0, make_uint4(w0[0], w0[1], w0[2], w0[3]));
-            __stcs(d0 + 1, make_uint4(w0[4], w0[5], w0[6], w0[7]));
-            __stcs(d1, make_uint4(w1[0], w1[1], w1[2], w1[3]));
-            __stcs(d1 + 1, make_uint4(w1[4], w1[5], w1[6], w1[7]));
-            if (qd == 0)
-                *reinterpret_cast<float2 *>(st + (m0 >> 7) * K + col) = make_float2(g0.s, g1.s);
-            // rare: words whose bracket disagreed get the exact quotient
-            while (redo != 0u) {
-                const int b2 = __ffs(redo) - 1;
-                redo &= redo - 1u;
-                const int hi = b2 >> 3, k = b2 & 7;
-                float v4[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int rr = 32 * qd + 4 * k + e;
-                    const uint32_t wv =
-                        reinterpret_cast<const uint32_t *>(&tl[rr][0])[(((p >> 2) ^ (rr & 15)) << 2) + (p & 3)];
-                    v4[e] = hi ? bf16_hi(wv) : bf16_lo(wv);
-                }
-                *reinterpret_cast<uint32_t *>(qt + (col + hi) * M + m0 + 32 * qd + 4 * k) =
-                    encode4_exact(v4[0], v4[1], v4[2], v4[3], hi ? g1.s : g0.s);
-            }
-        }
-        __syncthreads();                                // buffer `buf` is refilled two tiles on
     }
-    ptx::cp_async_wait<0>();
+    __syncthreads();
+
+    // ---- columns: chunk w, then w + 8 -------------------------------------
+    const int cq = lane & 3;                         // q: which row pairs of each 8-row block
+    const int cc = lane >> 2;                        // column within the 8-column chunk
+    uint8_t *stg = &sm.stage[warp][0][0];
+#pragma unroll 1
+    for (int pass = 0; pass < 2; ++pass) {
+        const int chunk = warp + 8 * pass;
+        uint32_t wv[16];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int r = 32 * j + lane;              // this lane's row address for the x4 load
+            uint32_t t4[4];
+            ldmatrix_x4_trans(t4, &sm.tile[r][chunk ^ (r & 15)]);
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+                wv[4 * j + m] = t4[m];               // rows 8(4j+m) + 2cq, +1 of column cc
+        }
+        float f[32];
+        float amax = 0.0f;
+#pragma unroll
+        for (int b = 0; b < 16; ++b) {
+            f[2 * b] = bf16_lo(wv[b]);
+            f[2 * b + 1] = bf16_hi(wv[b]);
+            amax = fmaxf(amax, fmaxf(fabsf(f[2 * b]), fabsf(f[2 * b + 1])));
+        }
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        const GroupScale gs = group_scale(amax);
+        uint32_t w[8];
+        const uint32_t redo = encode_words<8>(f, gs, w);
+        // rare: words whose bracket disagreed get the exact quotient (indices
+        // fixed at compile time, so f and w stay in registers)
+        if (redo != 0u) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                if (redo & (1u << k))
+                    w[k] = encode4_exact(f[4 * k], f[4 * k + 1], f[4 * k + 2], f[4 * k + 3], gs.s);
+        }
+        // word k holds rows 8(2k) + 2cq, +1 (low half) and 8(2k+1) + 2cq, +1 (high
+        // half): put each 2-byte unit at its row in the staged column
+        uint8_t *col = stg + cc * QD_STAGE_PITCH;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            *reinterpret_cast<uint16_t *>(col + 8 * (2 * k) + 2 * cq) = static_cast<uint16_t>(w[k]);
+            *reinterpret_cast<uint16_t *>(col + 8 * (2 * k + 1) + 2 * cq) = static_cast<uint16_t>(w[k] >> 16);
+        }
+        __syncwarp();
+        // lane 4c + q now takes rows 32q .. 32q+31 of column c: two 16-byte stores
+        const uint8_t *src = stg + cc * QD_STAGE_PITCH + 32 * cq;
+        const uint32_t *s32 = reinterpret_cast<const uint32_t *>(src);
+        const int64_t colg = k0 + 8 * chunk + cc;
+        uint4 *dst = reinterpret_cast<uint4 *>(qt + colg * M + m0 + 32 * cq);
+        __stcs(dst, make_uint4(s32[0], s32[1], s32[2], s32[3]));
+        __stcs(dst + 1, make_uint4(s32[4], s32[5], s32[6], s32[7]));
+        if (cq == 0)
+            st[(m0 >> 7) * K + colg] = gs.s;
+        __syncwarp();                                 // the staging buffer is reused next pass
+    }
 }
 
 }  // namespace
@@ -462,17 +462,12 @@ namespace jetfp8 {
 cudaError_t launch_quantize_act_dual(const void *x, int64_t M, int64_t K, uint8_t *q, float *s, uint8_t *qt,
                                      float *st, cudaStream_t stream)
 {
-    static_assert(sizeof(DualSmem) <= 227 * 1024 / QD_CTAS_PER_SM, "dual tile buffers exceed shared memory");
     cudaError_t e = cudaFuncSetAttribute(quantize_act_dual_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(sizeof(DualSmem)));
     if (e != cudaSuccess)
         return e;
-    int dev = 0, sms = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int64_t tiles = (M / QD_TILE) * (K / QD_TILE);
-    const int64_t grid = tiles < int64_t(sms) * QD_CTAS_PER_SM ? tiles : int64_t(sms) * QD_CTAS_PER_SM;
-    quantize_act_dual_kernel<<<static_cast<unsigned>(grid), QD_THREADS, sizeof(DualSmem), stream>>>(
+    quantize_act_dual_kernel<<<static_cast<unsigned>(tiles), QD_THREADS, sizeof(DualSmem), stream>>>(
         static_cast<const uint4 *>(x), M, K, q, s, qt, st);
     return cudaGetLastError();
 }

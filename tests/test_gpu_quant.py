@@ -260,3 +260,30 @@ def test_repeatable():
     a = jf.quantize_act(x)
     b = jf.quantize_act(x)
     assert all(torch.equal(u, v) for u, v in zip(a, b))
+
+
+def test_scale_for_every_bf16_amax():
+    """The group scale s = amax / 448 for every non-negative finite bf16
+    amax (the only values amax takes): row i holds the i-th pattern once and
+    zeros elsewhere; every kernel's scale must equal the oracle's IEEE
+    division, and the codes must match too."""
+    pats = np.arange(0, 0x7F80, dtype=np.uint16)
+    n = pats.size
+    rows = -(-n // 128) * 128
+    xb = np.zeros((rows, 128), dtype=np.uint16)
+    xb[:n, 7] = pats
+    xb[:n, 100] = pats >> 1                   # a second, smaller value in the group
+    x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16)
+    ox = oracle.quantize_act(xb, threads=ORACLE_THREADS)
+    q, s = jf.quantize_act(x.to(DEV))
+    assert_bitexact(q, ox[0], "codes")
+    assert_bitexact(s, ox[1], "scales")
+    # the same values down the columns, for the transposed and dual kernels
+    xt = x.t().contiguous()                   # [128, rows]: each column one group of 128 tokens
+    oxt = oracle.quantize_act_transposed(bits(xt), threads=ORACLE_THREADS)
+    qt, st = jf.quantize_act_transposed(xt.to(DEV))
+    assert_bitexact(qt, oxt[0], "transposed codes")
+    assert_bitexact(st, oxt[1], "transposed scales")
+    qd, sd, qdt, sdt = jf.quantize_act_dual(xt.to(DEV))
+    assert_bitexact(qdt, oxt[0], "dual transposed codes")
+    assert_bitexact(sdt, oxt[1], "dual transposed scales")

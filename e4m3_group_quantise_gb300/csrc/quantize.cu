@@ -350,19 +350,23 @@ quantize_act_dual_kernel(const uint4 *__restrict__ x, int64_t M, int64_t K, uint
             amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
             const GroupScale gs = group_scale(amax);
             uint32_t w[8];
-            const uint32_t redo = encode_words<8>(f, gs, w);
-            if (redo != 0u) {        // rare: the exact quotient for flagged words
-#pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    if (redo & (1u << k))
-                        w[k] = encode4_exact(f[4 * k], f[4 * k + 1], f[4 * k + 2], f[4 * k + 3], gs.s);
-            }
+            uint32_t redo = encode_words<8>(f, gs, w);
             uint8_t *row_q = q + (m0 + r) * K + k0;
 #pragma unroll
             for (int j = 0; j < 4; ++j)      // the row's four lanes write 32 contiguous bytes per j
                 *reinterpret_cast<uint2 *>(row_q + 8 * (sub + 4 * j)) = make_uint2(w[2 * j], w[2 * j + 1]);
             if (sub == 0)
                 s[(k0 >> 7) * M + m0 + r] = gs.s;
+            // rare: a word whose bracket disagreed gets the exact quotient, its
+            // four inputs re-read from the shared tile (word k: chunk sub + 4(k/2),
+            // half k%2)
+            while (redo != 0u) {
+                const int k = __ffs(redo) - 1;
+                redo &= redo - 1u;
+                const int c = sub + 4 * (k >> 1);
+                const uint2 in = reinterpret_cast<const uint2 *>(&sm.tile[r][c ^ (r & 15)])[k & 1];
+                *reinterpret_cast<uint32_t *>(row_q + 8 * c + 4 * (k & 1)) = encode4_exact(in, gs.s);
+            }
         }
     }
     __syncthreads();
@@ -396,15 +400,7 @@ quantize_act_dual_kernel(const uint4 *__restrict__ x, int64_t M, int64_t K, uint
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
         const GroupScale gs = group_scale(amax);
         uint32_t w[8];
-        const uint32_t redo = encode_words<8>(f, gs, w);
-        // rare: words whose bracket disagreed get the exact quotient (indices
-        // fixed at compile time, so f and w stay in registers)
-        if (redo != 0u) {
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                if (redo & (1u << k))
-                    w[k] = encode4_exact(f[4 * k], f[4 * k + 1], f[4 * k + 2], f[4 * k + 3], gs.s);
-        }
+        uint32_t redo = encode_words<8>(f, gs, w);
         // word k holds rows 8(2k) + 2cq, +1 (low half) and 8(2k+1) + 2cq, +1 (high
         // half): put each 2-byte unit at its row in the staged column
         uint8_t *col = stg + cc * QD_STAGE_PITCH;
@@ -412,6 +408,27 @@ quantize_act_dual_kernel(const uint4 *__restrict__ x, int64_t M, int64_t K, uint
         for (int k = 0; k < 8; ++k) {
             *reinterpret_cast<uint16_t *>(col + 8 * (2 * k) + 2 * cq) = static_cast<uint16_t>(w[k]);
             *reinterpret_cast<uint16_t *>(col + 8 * (2 * k + 1) + 2 * cq) = static_cast<uint16_t>(w[k] >> 16);
+        }
+        // rare: a word whose bracket disagreed gets the exact quotient, its four
+        // inputs (rows 16k + 2cq, +1, 16k + 8 + 2cq, +1 of the column) re-read
+        // from the shared tile; the fixed units overwrite the staged ones
+        {
+            const int colw = 8 * chunk + cc;          // column within the tile
+            while (redo != 0u) {
+                const int k = __ffs(redo) - 1;
+                redo &= redo - 1u;
+                float v4[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int rr = 16 * k + 8 * (e >> 1) + 2 * cq + (e & 1);
+                    const uint16_t h =
+                        reinterpret_cast<const uint16_t *>(&sm.tile[rr][chunk ^ (rr & 15)])[colw & 7];
+                    v4[e] = __uint_as_float(static_cast<uint32_t>(h) << 16);
+                }
+                const uint32_t fixed = encode4_exact(v4[0], v4[1], v4[2], v4[3], gs.s);
+                *reinterpret_cast<uint16_t *>(col + 16 * k + 2 * cq) = static_cast<uint16_t>(fixed);
+                *reinterpret_cast<uint16_t *>(col + 16 * k + 8 + 2 * cq) = static_cast<uint16_t>(fixed >> 16);
+            }
         }
         __syncwarp();
         // lane 4c + q now takes rows 32q .. 32q+31 of column c: two 16-byte stores

@@ -356,16 +356,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                         const bool in = row < args.rows;
                         ptx::cp_async_4(dst + r, in ? sa_g + row : args.sa, in ? 4u : 0u);
                     }
+                    // the block scales of the tile's 128-column blocks (per-column
+                    // scales never come here: the TMA producer copies those)
                     const float *sb_g = args.sb + static_cast<int64_t>(g) * args.sb_stride_g;
-                    if (SB_PER_COLUMN) {
-#pragma unroll
-                        for (int i = 0; i < BN / 128; ++i) {         // BN/4 16-byte pieces per slot
-                            const int c = (i * 32 + lane) * 4;
-                            const int col = tn * BN + c;
-                            const bool in = col < args.cols;
-                            ptx::cp_async_16z(dst + BM + c, in ? sb_g + col : args.sb, in ? 16u : 0u);
-                        }
-                    } else if (lane < (BN >= 128 ? BN / 128 : 1)) {
+                    if (lane < (BN >= 128 ? BN / 128 : 1)) {
                         const int col = tn * BN + lane * 128;
                         const bool in = col < args.cols;
                         ptx::cp_async_4(dst + BM + lane,

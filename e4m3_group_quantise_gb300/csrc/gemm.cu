@@ -150,6 +150,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     // eight for narrow (decode) tiles, so that the MMAs can run up to eight
     // groups ahead of the read-back instead of waiting on every hand-off.
     constexpr uint32_t NBUF = PAIR ? 4 : (BN >= 128 ? 2 : MAX_TBUF);
+    // Narrow tiles: the MMA issuer, whose loop sets their pace, commits only
+    // the TMEM-full barrier; its completion also means the group's MMAs have
+    // read their shared-memory stage, and the first promotion warp, seeing
+    // it, releases the stage to the producer.  (Wide tiles keep the separate
+    // commit: their read-back lags the MMAs and would hold the stages.)
+    constexpr bool PROMO_RELEASES_STAGE = BN < 128 && !PAIR;
     constexpr uint32_t TMEM_COLS = NBUF * BN;
     static_assert(TMEM_COLS <= 512, "TMEM holds 512 columns");
     constexpr uint32_t IDESC = ptx::idesc_e4m3_f32(BM, BN);
@@ -319,7 +325,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                             ptx::mma_f8(d_tmem, adesc + 2 * j, bdesc + 2 * j, IDESC, j > 0 ? 1u : 0u);
                         if (PAIR)
                             ptx::mma_commit_multicast(&empty[stage], 0x3);
-                        else
+                        else if (!PROMO_RELEASES_STAGE)
                             ptx::mma_commit(&empty[stage]);
                         ptx::mma_commit(&tfull[buf]);
                         if (++stage == STAGES) {
@@ -426,6 +432,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                     break;
                 }
                 ptx::tc_fence_after();
+                if (PROMO_RELEASES_STAGE && warp == FIRST_PROMO_WARP && lane == 0)
+                    ptx::mbar_arrive(&empty[it % STAGES]);      // the group's MMAs are done with it
                 const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + buf * BN +
                                        wg * COLS_PER_WG;
                 // acc += partial * scale for 32 columns starting at column c0

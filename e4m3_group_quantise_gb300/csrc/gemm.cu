@@ -156,6 +156,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     // it, releases the stage to the producer.  (Wide tiles keep the separate
     // commit: their read-back lags the MMAs and would hold the stages.)
     constexpr bool PROMO_RELEASES_STAGE = BN < 128 && !PAIR;
+    // Narrow tiles also get a second MMA issuer (the otherwise idle fourth
+    // control warp): even groups from the MMA warp, odd groups from warp 3,
+    // into different TMEM buffers, so the two issue loops overlap.
+    constexpr bool TWO_ISSUERS = PROMO_RELEASES_STAGE;
+    constexpr int SECOND_MMA_WARP = 3;
     constexpr uint32_t TMEM_COLS = NBUF * BN;
     static_assert(TMEM_COLS <= 512, "TMEM holds 512 columns");
     constexpr uint32_t IDESC = ptx::idesc_e4m3_f32(BM, BN);
@@ -205,7 +210,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                 ptx::mbar_init(&tfull[b], 1);
                 ptx::mbar_init(&tempty[b], 4 * NWG);   // one arrival per promotion warp
             }
-            ptx::mbar_init(mma_done, 1);
+            ptx::mbar_init(mma_done, TWO_ISSUERS ? 2 : 1);   // one final commit per MMA issuer
             *abort_flag = 0;
             ptx::fence_mbar_init();
             ptx::tma_prefetch_desc(&tmap_a);
@@ -296,17 +301,20 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                 }
             }
             __syncwarp();
-        } else if (warp == MMA_WARP) {
-            // -------------------------------------------------- MMA issuer
+        } else if (warp == MMA_WARP || (TWO_ISSUERS && warp == SECOND_MMA_WARP)) {
+            // -------------------------------------------------- MMA issuer(s)
             if (lane == 0) {
-                int stage = 0;
-                uint32_t phase = 0;
-                uint32_t it = 0;   // global group counter -> TMEM buffer / phase
+                const uint32_t parity = warp == MMA_WARP ? 0u : 1u;   // groups this issuer takes
+                uint32_t it = 0;   // global group counter -> smem stage, TMEM buffer, phases
                 bool ok = true;
                 const uint32_t a_base = ptx::smem_u32(sA);
                 const uint32_t b_base = ptx::smem_u32(sB);
                 for (int tile = work_first; ok && tile < num_work; tile += work_stride) {
                     for (int g = 0; g < G; ++g, ++it) {
+                        if (TWO_ISSUERS && (it & 1u) != parity)
+                            continue;
+                        const int stage = static_cast<int>(it % STAGES);
+                        const uint32_t phase = (it / STAGES) & 1u;
                         const uint32_t buf = it % NBUF;
                         const uint32_t bphase = (it / NBUF) & 1u;
                         if (!ptx::mbar_wait(&tempty[buf], bphase ^ 1u, abort_flag, args.err, ERRBIT_MMA_TMEM,
@@ -328,10 +336,6 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                         else if (!PROMO_RELEASES_STAGE)
                             ptx::mma_commit(&empty[stage]);
                         ptx::mma_commit(&tfull[buf]);
-                        if (++stage == STAGES) {
-                            stage = 0;
-                            phase ^= 1u;
-                        }
                     }
                 }
                 // all MMAs issued by this thread complete before teardown

@@ -146,17 +146,19 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     constexpr int CHUNKS = COLS_PER_WG / 32;     // tcgen05.ld x32 per group
     constexpr int LPW = CHUNKS >= 2 ? 2 : 1;     // loads in flight per wait
     static_assert(CHUNKS % LPW == 0, "loads are issued in pairs");
-    // TMEM partial buffers: two 256- or 128-wide ones, four for CTA pairs,
-    // eight for narrow (decode) tiles, so that the MMAs can run up to eight
-    // groups ahead of the read-back instead of waiting on every hand-off.
-    constexpr uint32_t NBUF = PAIR ? 4 : (BN >= 128 ? 2 : MAX_TBUF);
-    // Narrow tiles: the MMA issuer, whose loop sets their pace, commits only
-    // the TMEM-full barrier; its completion also means the group's MMAs have
-    // read their shared-memory stage, and the first promotion warp, seeing
-    // it, releases the stage to the producer.  (Wide tiles keep the separate
-    // commit: their read-back lags the MMAs and would hold the stages.)
-    constexpr bool PROMO_RELEASES_STAGE = BN < 128 && !PAIR;
-    // Narrow tiles also get a second MMA issuer (the otherwise idle fourth
+    // TMEM partial buffers: two 256-wide ones; four 128-wide ones (also for
+    // CTA pairs); eight for narrower (decode) tiles, so that the MMAs can run
+    // several groups ahead of the read-back instead of waiting on every
+    // hand-off.
+    constexpr uint32_t NBUF = PAIR ? 4 : (BN >= 256 ? 2 : (BN == 128 ? 4 : MAX_TBUF));
+    // Tiles up to 128 wide (problems too small for 256-wide tiles): the MMA
+    // issuer, whose loop sets their pace, commits only the TMEM-full barrier;
+    // its completion also means the group's MMAs have read their shared-memory
+    // stage, and the first promotion warp, seeing it, releases the stage to
+    // the producer.  (256-wide tiles keep the separate commit: their read-back
+    // lags the MMAs and would hold the stages.)
+    constexpr bool PROMO_RELEASES_STAGE = BN <= 128 && !PAIR;
+    // Those tiles also get a second MMA issuer (the otherwise idle fourth
     // control warp): even groups from the MMA warp, odd groups from warp 3,
     // into different TMEM buffers, so the two issue loops overlap.
     constexpr bool TWO_ISSUERS = PROMO_RELEASES_STAGE;

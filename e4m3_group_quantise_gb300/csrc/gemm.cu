@@ -158,10 +158,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     // the producer.  (256-wide tiles keep the separate commit: their read-back
     // lags the MMAs and would hold the stages.)
     constexpr bool PROMO_RELEASES_STAGE = BN <= 128 && !PAIR;
-    // Those tiles also get a second MMA issuer (the otherwise idle fourth
-    // control warp): even groups from the MMA warp, odd groups from warp 3,
-    // into different TMEM buffers, so the two issue loops overlap.
-    constexpr bool TWO_ISSUERS = PROMO_RELEASES_STAGE;
+    // A second MMA issuer (the otherwise idle fourth control warp): even
+    // groups from the MMA warp, odd groups from warp 3, into different TMEM
+    // buffers, so one group's MMAs are issued as soon as its buffer is free
+    // rather than after the previous group's issue loop (the issue of a
+    // group's four MMAs and commits takes a few hundred cycles).
+    constexpr bool TWO_ISSUERS = !PAIR;
     constexpr int SECOND_MMA_WARP = 3;
     constexpr uint32_t TMEM_COLS = NBUF * BN;
     static_assert(TMEM_COLS <= 512, "TMEM holds 512 columns");

@@ -21,27 +21,30 @@
 //
 // Structure: persistent, one CTA per SM, 384 threads (3 warpgroups).
 //   warp 0, lane 0 : TMA producer   -- A and B tiles of one group per smem stage
-//   warp 1, lane 0 : MMA issuer     -- 4 x tcgen05.mma (K = 32 each) per group
-//                                      into one of two TMEM partial buffers
+//   warps 1 and 3,  : MMA issuers   -- even and odd groups: 4 x tcgen05.mma
+//   lane 0                             (K = 32 each) per group into one of the
+//                                      TMEM partial buffers
 //   warp 2         : scale loader   -- cp.async of the group's row scales (128)
 //                                      and block scales into a smem ring (with
 //                                      per-column scales, both contiguous, the
 //                                      TMA producer fetches them instead, two
 //                                      bulk copies per group)
 //   warps 4..11    : promotion      -- two warpgroups, each 128 rows x BN/2
-//                                      columns; tcgen05.ld the partial, free the
-//                                      buffer, acc += partial * sa * sb (packed
-//                                      fp32x2 FMAs); bf16 epilogue: each warp
+//                                      columns (narrow tiles: the first alone);
+//                                      tcgen05.ld the partial, free the buffer,
+//                                      acc += partial * sa * sb (packed fp32x2
+//                                      operations); bf16 epilogue: each warp
 //                                      stages 32 rows x 16 columns in shared
 //                                      memory and TMA-stores them (double-
 //                                      buffered, asynchronous)
 // Registers are rebalanced with setmaxnreg (RegSplit): with 128 x 256 tiles
 // the control warpgroup drops to 40 per thread and the promotion warpgroups
 // rise to 232 (128*40 + 256*232 = 64512 = 384 threads * 168, the launch
-// allocation).  Tile BM = 128 rows x BN (256, or 128 for small problems)
-// columns; one pipeline stage per 128-wide K group (the scale granularity).  Every wait is bounded: a
-// wait that runs out sets the device error word, the CTA drains its copies
-// and MMAs in flight, frees its tensor memory and exits.
+// allocation).  Tile BM = 128 rows x BN (256; 128, 64 or 32 for problems with
+// few tiles) columns; one pipeline stage per 128-wide K group (the scale
+// granularity).  Every wait is bounded: a wait that runs out sets the device
+// error word, the CTA drains its copies and MMAs in flight, frees its tensor
+// memory and exits.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
@@ -125,6 +128,10 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// 16x256b TMEM loads of 64 or 32 columns, chosen by the register array
+__device__ __forceinline__ void tmem_ld_quads(uint32_t taddr, uint32_t (&r)[32]) { ptx::tmem_ld_16x256b_x8(taddr, r); }
+__device__ __forceinline__ void tmem_ld_quads(uint32_t taddr, uint32_t (&r)[16]) { ptx::tmem_ld_16x256b_x4(taddr, r); }
+
 // PAIR: the kernel runs as clusters of two CTAs that compute horizontally
 // adjacent 128 x BN tiles (same rows).  Each CTA loads half of the shared A
 // tile and multicasts it to both; a stage is refilled only after both CTAs'
@@ -146,6 +153,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     constexpr int CHUNKS = COLS_PER_WG / 32;     // tcgen05.ld x32 per group
     constexpr int LPW = CHUNKS >= 2 ? 2 : 1;     // loads in flight per wait
     static_assert(CHUNKS % LPW == 0, "loads are issued in pairs");
+    // Per-column scales (Wgrad) read the partial as 16x256b quads instead:
+    // a thread then holds four rows x a quarter of the columns, so each
+    // column-scale pair it fetches from shared memory serves four rows.
+    // The range is read in slabs of up to 64 columns (8 blocks of 8), both
+    // 16-lane halves of the warp's quarter per slab.
+    constexpr int CB = COLS_PER_WG / 8;          // 8-column blocks per warpgroup
+    constexpr int SLAB = CB >= 8 ? 8 : CB;       // blocks per slab
+    constexpr int NSLAB = CB / SLAB;
+    static_assert(CB % SLAB == 0 && (SLAB == 8 || SLAB == 4), "slabs of 64 or 32 columns");
     // TMEM partial buffers: two 256-wide ones; four 128-wide ones (also for
     // CTA pairs); eight for narrower (decode) tiles, so that the MMAs can run
     // several groups ahead of the read-back instead of waiting on every
@@ -405,17 +421,19 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
             int tm, tn;
             coords(tile, tm, tn);
             const int col0 = tn * BN + wg * COLS_PER_WG;
-            // fp32 accumulators of this thread's row: packed pairs (columns 2i,
-            // 2i+1) with one scale per 128-column block, plain floats with a
-            // scale per column
+            // fp32 accumulators as packed pairs of adjacent columns: with one
+            // scale per 128-column block, this thread's row (pair i = columns
+            // 2i, 2i+1); with a scale per column, four rows r = 8k + lane/4 of
+            // the warp's 32 (k = 0..3) at columns 8b + 2(lane%4) + {0, 1} of
+            // each 8-column block b (pair k * CB + b)
             uint64_t acc2[SB_PER_COLUMN ? 1 : COLS_PER_WG / 2];
-            float acc1[SB_PER_COLUMN ? COLS_PER_WG : 1];
+            uint64_t accp[SB_PER_COLUMN ? COLS_PER_WG / 2 : 1];
 #pragma unroll
             for (int i = 0; i < (SB_PER_COLUMN ? 1 : COLS_PER_WG / 2); ++i)
                 acc2[i] = 0ull;
 #pragma unroll
-            for (int i = 0; i < (SB_PER_COLUMN ? COLS_PER_WG : 1); ++i)
-                acc1[i] = 0.0f;
+            for (int i = 0; i < (SB_PER_COLUMN ? COLS_PER_WG / 2 : 1); ++i)
+                accp[i] = 0ull;
 
             for (int g = 0; g < G; ++g, ++it) {
                 const uint32_t buf = it % NBUF;
@@ -425,11 +443,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                     break;
                 }
                 const float *scur = scl + ss * L::SCALE_FLOATS;
-                const float sa = scur[row_in_tile];
                 const float *sbcol = scur + BM + wg * COLS_PER_WG;
                 float w_blk = 0.0f;
                 if (!SB_PER_COLUMN) {
-                    w_blk = sa * scur[BM + (wg * COLS_PER_WG) / 128];
+                    w_blk = scur[row_in_tile] * scur[BM + (wg * COLS_PER_WG) / 128];
                     __syncwarp();
                     if (lane == 0)
                         ptx::mbar_arrive(&sempty[ss]);
@@ -444,51 +461,76 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                     ptx::mbar_arrive(&empty[it % STAGES]);      // the group's MMAs are done with it
                 const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + buf * BN +
                                        wg * COLS_PER_WG;
-                // acc += partial * scale for 32 columns starting at column c0
-                // of this warpgroup's range
-                auto apply32 = [&](const uint32_t(&p)[32], const int c0) {
-                    if (SB_PER_COLUMN) {
-                        // acc += p * (sa * sb[col]): the products two at a time,
-                        // the accumulation in plain fp32 FMAs
-                        const uint64_t sa2 = ptx::pack_f32x2(sa, sa);
-                        const uint64_t *sbv = reinterpret_cast<const uint64_t *>(sbcol + c0);
-                        float *a = acc1 + c0;
+                if (SB_PER_COLUMN) {
+                    // acc += p * (sa[row] * sb[col]), two columns at a time
+                    // (packed fp32 multiply and fused multiply-add, each lane
+                    // rounded as the scalar operation would be)
+                    const int cq = 2 * (lane & 3);
+                    uint64_t sa2[4];
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const uint64_t w = ptx::mul_f32x2(sa2, sbv[i]);
-                            a[2 * i] = fmaf(__uint_as_float(p[2 * i]), ptx::lo_f32(w), a[2 * i]);
-                            a[2 * i + 1] = fmaf(__uint_as_float(p[2 * i + 1]), ptx::hi_f32(w), a[2 * i + 1]);
+                    for (int k = 0; k < 4; ++k) {
+                        const float v = scur[quarter * 32 + 8 * k + (lane >> 2)];
+                        sa2[k] = ptx::pack_f32x2(v, v);
+                    }
+#pragma unroll
+                    for (int j = 0; j < NSLAB; ++j) {
+                        uint32_t p0[4 * SLAB], p1[4 * SLAB];   // lanes 0-15 and 16-31 of the quarter
+                        tmem_ld_quads(taddr + j * 8 * SLAB, p0);
+                        tmem_ld_quads(taddr + (16u << 16) + j * 8 * SLAB, p1);
+                        ptx::tmem_ld_wait(p0);
+                        ptx::tmem_ld_wait(p1);
+                        if (j + 1 == NSLAB) {
+                            // the whole partial is in registers: hand the buffer back
+                            ptx::tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0)
+                                ptx::mbar_arrive(&tempty[buf]);
                         }
-                    } else {
+#pragma unroll
+                        for (int i = 0; i < SLAB; ++i) {
+                            const int b = j * SLAB + i;
+                            const uint64_t sb2 = *reinterpret_cast<const uint64_t *>(sbcol + 8 * b + cq);
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                const uint32_t *p = (k < 2 ? p0 : p1) + 4 * i + 2 * (k & 1);
+                                const uint64_t w = ptx::mul_f32x2(sa2[k], sb2);
+                                ptx::fma_f32x2(accp[k * CB + b], ptx::pack_f32x2(p[0], p[1]), w);
+                            }
+                        }
+                    }
+                } else {
+                    // acc += partial * (sa * sb) for 32 columns starting at
+                    // column c0 of this warpgroup's range; two 32-column loads
+                    // in flight per wait (64 columns) where the range allows,
+                    // so each group pays the TMEM load latency only
+                    // COLS_PER_WG / 64 times
+                    auto apply32 = [&](const uint32_t(&p)[32], const int c0) {
                         const uint64_t w2 = ptx::pack_f32x2(w_blk, w_blk);
                         uint64_t *a0 = acc2 + c0 / 2;
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
                             ptx::fma_f32x2(a0[i], ptx::pack_f32x2(p[2 * i], p[2 * i + 1]), w2);
-                    }
-                };
-                // Two 32-column loads in flight per wait (64 columns) where the
-                // warpgroup's range allows, so each group pays the TMEM load
-                // latency only COLS_PER_WG / 64 times.
+                    };
 #pragma unroll
-                for (int h = 0; h < CHUNKS / LPW; ++h) {
-                    uint32_t p0[32], p1[32];
-                    ptx::tmem_ld_32x32b_x32(taddr + h * 32 * LPW, p0);
-                    if (LPW == 2)
-                        ptx::tmem_ld_32x32b_x32(taddr + h * 64 + 32, p1);
-                    ptx::tmem_ld_wait(p0);
-                    if (LPW == 2)
-                        ptx::tmem_ld_wait(p1);
-                    if (h + 1 == CHUNKS / LPW) {
-                        // the whole partial is in registers: hand the buffer back
-                        ptx::tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0)
-                            ptx::mbar_arrive(&tempty[buf]);
+                    for (int h = 0; h < CHUNKS / LPW; ++h) {
+                        uint32_t p0[32], p1[32];
+                        ptx::tmem_ld_32x32b_x32(taddr + h * 32 * LPW, p0);
+                        if (LPW == 2)
+                            ptx::tmem_ld_32x32b_x32(taddr + h * 64 + 32, p1);
+                        ptx::tmem_ld_wait(p0);
+                        if (LPW == 2)
+                            ptx::tmem_ld_wait(p1);
+                        if (h + 1 == CHUNKS / LPW) {
+                            // the whole partial is in registers: hand the buffer back
+                            ptx::tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0)
+                                ptx::mbar_arrive(&tempty[buf]);
+                        }
+                        apply32(p0, h * 32 * LPW);
+                        if (LPW == 2)
+                            apply32(p1, h * 64 + 32);
                     }
-                    apply32(p0, h * 32 * LPW);
-                    if (LPW == 2)
-                        apply32(p1, h * 64 + 32);
                 }
                 if (SB_PER_COLUMN) {
                     __syncwarp();
@@ -512,23 +554,34 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                     if (lane == 0)
                         ptx::bulk_wait_read<1>();          // the store that last used this buffer has read it
                     __syncwarp();
-                    uint4 *dst = reinterpret_cast<uint4 *>(chunk + lane * 32);
-                    uint4 o0, o1;
-                    float v[16];
+                    if (SB_PER_COLUMN) {
+                        // chunk c is blocks 2c and 2c+1; a row of the chunk is 32 bytes
 #pragma unroll
-                    for (int k = 0; k < 16; ++k)
-                        v[k] = SB_PER_COLUMN ? acc1[16 * c + k]
-                                             : ((k & 1) ? ptx::hi_f32(acc2[8 * c + k / 2]) : ptx::lo_f32(acc2[8 * c + k / 2]));
-                    o0.x = pack_bf16x2(v[0], v[1]);
-                    o0.y = pack_bf16x2(v[2], v[3]);
-                    o0.z = pack_bf16x2(v[4], v[5]);
-                    o0.w = pack_bf16x2(v[6], v[7]);
-                    o1.x = pack_bf16x2(v[8], v[9]);
-                    o1.y = pack_bf16x2(v[10], v[11]);
-                    o1.z = pack_bf16x2(v[12], v[13]);
-                    o1.w = pack_bf16x2(v[14], v[15]);
-                    dst[0] = o0;
-                    dst[1] = o1;
+                        for (int k = 0; k < 4; ++k)
+#pragma unroll
+                            for (int e = 0; e < 2; ++e) {
+                                const uint64_t a = accp[k * CB + 2 * c + e];
+                                *reinterpret_cast<uint32_t *>(chunk + (8 * k + (lane >> 2)) * 32 + e * 16 +
+                                                              (lane & 3) * 4) = pack_bf16x2(ptx::lo_f32(a), ptx::hi_f32(a));
+                            }
+                    } else {
+                        uint4 *dst = reinterpret_cast<uint4 *>(chunk + lane * 32);
+                        uint4 o0, o1;
+                        float v[16];
+#pragma unroll
+                        for (int k = 0; k < 16; ++k)
+                            v[k] = (k & 1) ? ptx::hi_f32(acc2[8 * c + k / 2]) : ptx::lo_f32(acc2[8 * c + k / 2]);
+                        o0.x = pack_bf16x2(v[0], v[1]);
+                        o0.y = pack_bf16x2(v[2], v[3]);
+                        o0.z = pack_bf16x2(v[4], v[5]);
+                        o0.w = pack_bf16x2(v[6], v[7]);
+                        o1.x = pack_bf16x2(v[8], v[9]);
+                        o1.y = pack_bf16x2(v[10], v[11]);
+                        o1.z = pack_bf16x2(v[12], v[13]);
+                        o1.w = pack_bf16x2(v[14], v[15]);
+                        dst[0] = o0;
+                        dst[1] = o1;
+                    }
                     ptx::fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {

@@ -110,6 +110,14 @@ def test_wgrad_shapes(M, N, K):
     run_wgrad(M, N, K, M + K)
 
 
+@pytest.mark.parametrize("M,N,K", [(384, 1024, 1024), (256, 2048, 1024), (128, 128, 4096)])
+def test_wgrad_tile_widths(M, N, K):
+    """Wgrad problems whose tile count makes the launcher pick 64-, 128- and
+    32-wide tiles (output 1024 x 1024: 64; 2048 x 1024: 128; 128 x 4096: 32),
+    each a different slab layout of the per-column-scale read-back."""
+    run_wgrad(M, N, K, M + N + K)
+
+
 def test_many_tiles_persistent_loop():
     """More tiles than SMs on every variant (each CTA walks several tiles)."""
     run_fprop(2048, 4096, 512, 5, sample=2048)

@@ -156,12 +156,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     // Per-column scales (Wgrad) read the partial as 16x256b quads instead:
     // a thread then holds four rows x a quarter of the columns, so each
     // column-scale pair it fetches from shared memory serves four rows.
-    // The range is read in slabs of up to 64 columns (8 blocks of 8), both
-    // 16-lane halves of the warp's quarter per slab.
+    // The range is read in slabs of 32 columns (4 blocks of 8), both 16-lane
+    // halves of the warp's quarter per slab, the next slab's load in flight
+    // while this one is scaled (Wgrad +3 % against two unpipelined 64-column
+    // slabs; the same pipelining of the 32x32b loads measured 19 % slower for
+    // Fprop, whose arithmetic per slab is too short to hide a load).
     constexpr int CB = COLS_PER_WG / 8;          // 8-column blocks per warpgroup
-    constexpr int SLAB = CB >= 8 ? 8 : CB;       // blocks per slab
-    constexpr int NSLAB = CB / SLAB;
-    static_assert(CB % SLAB == 0 && (SLAB == 8 || SLAB == 4), "slabs of 64 or 32 columns");
+    constexpr int PS = 4;                        // blocks per slab
+    constexpr int NPS = CB / PS;                 // slabs per group
+    static_assert(CB % PS == 0, "32-column slabs");
     // TMEM partial buffers: two 256-wide ones; four 128-wide ones (also for
     // CTA pairs); eight for narrower (decode) tiles, so that the MMAs can run
     // several groups ahead of the read-back instead of waiting on every
@@ -472,14 +475,19 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                         const float v = scur[quarter * 32 + 8 * k + (lane >> 2)];
                         sa2[k] = ptx::pack_f32x2(v, v);
                     }
+                    uint32_t q0[NPS][16], q1[NPS][16];   // lanes 0-15 and 16-31 of the quarter
+                    tmem_ld_quads(taddr, q0[0]);
+                    tmem_ld_quads(taddr + (16u << 16), q1[0]);
 #pragma unroll
-                    for (int j = 0; j < NSLAB; ++j) {
-                        uint32_t p0[4 * SLAB], p1[4 * SLAB];   // lanes 0-15 and 16-31 of the quarter
-                        tmem_ld_quads(taddr + j * 8 * SLAB, p0);
-                        tmem_ld_quads(taddr + (16u << 16) + j * 8 * SLAB, p1);
-                        ptx::tmem_ld_wait(p0);
-                        ptx::tmem_ld_wait(p1);
-                        if (j + 1 == NSLAB) {
+                    for (int j = 0; j < NPS; ++j) {
+                        ptx::tmem_ld_wait(q0[j]);
+                        ptx::tmem_ld_wait(q1[j]);
+                        if (j + 1 < NPS) {
+                            tmem_ld_quads(taddr + (j + 1) * 8 * PS, q0[j + 1]);
+                            tmem_ld_quads(taddr + (16u << 16) + (j + 1) * 8 * PS, q1[j + 1]);
+                        }
+                        const uint32_t *p0 = q0[j], *p1 = q1[j];
+                        if (j + 1 == NPS) {
                             // the whole partial is in registers: hand the buffer back
                             ptx::tc_fence_before();
                             __syncwarp();
@@ -487,8 +495,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                                 ptx::mbar_arrive(&tempty[buf]);
                         }
 #pragma unroll
-                        for (int i = 0; i < SLAB; ++i) {
-                            const int b = j * SLAB + i;
+                        for (int i = 0; i < PS; ++i) {
+                            const int b = j * PS + i;
                             const uint64_t sb2 = *reinterpret_cast<const uint64_t *>(sbcol + 8 * b + cq);
 #pragma unroll
                             for (int k = 0; k < 4; ++k) {

@@ -27,39 +27,56 @@ namespace {
 constexpr int PR_THREADS = 256;
 constexpr int PR_WARPS = PR_THREADS / 32;
 
-__device__ __forceinline__ float pow2_normal(int k)   // 2^k, -126 <= k <= 127
+// 2^k for -126 <= k <= 127 (unsigned arithmetic: other k, from lanes whose
+// result is discarded, give some bit pattern without overflow)
+__device__ __forceinline__ float pow2_normal(int k)
 {
-    return __int_as_float((k + 127) << 23);
+    return __uint_as_float((static_cast<uint32_t>(k) + 127u) << 23);
 }
 
-// e^x in fp32: Cody-Waite range reduction x = n ln2 + r with
-// n = rint(x / ln2), |r| <= ln2 / 2; e^r from its degree-7 Taylor polynomial
-// in Horner form with fused multiply-adds; then the scaling by 2^n in two
-// exact steps.  ln2 is split into a head with 16 significant bits (45426 /
-// 2^16, so n * head is exact) and the rounded remainder.  x >= 89 gives
-// +inf, x < -87 gives +0.
-__device__ __forceinline__ float exp_f32(float x)
+// e^x in fp32 for two values at once: Cody-Waite range reduction
+// x = n ln2 + r with n = rint(x / ln2), |r| <= ln2 / 2; e^r from its degree-7
+// Taylor polynomial in Horner form with fused multiply-adds; then the scaling
+// by 2^n in two exact steps.  ln2 is split into a head with 16 significant
+// bits (45426 / 2^16, so n * head is exact) and the rounded remainder.
+// x >= 89 gives +inf, x < -87 gives +0, NaN stays NaN.  Every multiply and
+// fused multiply-add is one packed fp32x2 operation, whose lanes round
+// exactly as the scalar operation would (fma(-n, c, x) is written
+// fma(n, -c, x): the same product, the same rounding); lanes outside the
+// range are replaced at the end.
+__device__ __forceinline__ void exp_f32x2(float x0, float x1, float &e0, float &e1)
 {
-    if (x != x)
-        return x;
-    if (x >= 89.0f)
-        return __int_as_float(0x7f800000);
-    if (x < -87.0f)
-        return 0.0f;
-    const float n = rintf(__fmul_rn(x, 1.44269502f));   // fp32(1 / ln 2)
-    float r = fmaf(-n, 0.693145751953125f, x);           // 45426 / 65536
-    r = fmaf(-n, 1.42860677e-06f, r);                    // fp32(ln 2 - 45426 / 65536)
-    float p = 0.000198412701f;                           // fp32(1 / k!), k = 7 .. 2
-    p = fmaf(p, r, 0.00138888892f);
-    p = fmaf(p, r, 0.00833333377f);
-    p = fmaf(p, r, 0.0416666679f);
-    p = fmaf(p, r, 0.166666672f);
-    p = fmaf(p, r, 0.5f);
-    p = fmaf(p, r, 1.0f);
-    p = fmaf(p, r, 1.0f);
-    const int ni = static_cast<int>(n);                  // -126 .. 128
-    const int n1 = ni / 2;
-    return __fmul_rn(__fmul_rn(p, pow2_normal(n1)), pow2_normal(ni - n1));
+    using namespace ptx;
+    auto dup = [](float c) { return pack_f32x2(c, c); };
+    const uint64_t x = pack_f32x2(x0, x1);
+    const uint64_t t = mul_f32x2(x, dup(1.44269502f));
+    const float n0 = rintf(lo_f32(t)), n1 = rintf(hi_f32(t));
+    const uint64_t n = pack_f32x2(n0, n1);
+    uint64_t r = fma2_f32x2(n, dup(-0.693145751953125f), x);
+    r = fma2_f32x2(n, dup(-1.42860677e-06f), r);
+    uint64_t p = fma2_f32x2(dup(0.000198412701f), r, dup(0.00138888892f));
+    p = fma2_f32x2(p, r, dup(0.00833333377f));
+    p = fma2_f32x2(p, r, dup(0.0416666679f));
+    p = fma2_f32x2(p, r, dup(0.166666672f));
+    p = fma2_f32x2(p, r, dup(0.5f));
+    p = fma2_f32x2(p, r, dup(1.0f));
+    p = fma2_f32x2(p, r, dup(1.0f));
+    const int i0 = __float2int_rz(n0), i1 = __float2int_rz(n1);   // exact in range, saturating outside
+    const int h0 = i0 / 2, h1 = i1 / 2;
+    const uint64_t s1 = pack_f32x2(pow2_normal(h0), pow2_normal(h1));
+    const uint64_t s2 = pack_f32x2(pow2_normal(i0 - h0), pow2_normal(i1 - h1));
+    const uint64_t e = mul_f32x2(mul_f32x2(p, s1), s2);
+    auto fix = [](float xv, float ev) {
+        if (xv != xv)
+            return xv;
+        if (xv >= 89.0f)
+            return __int_as_float(0x7f800000);
+        if (xv < -87.0f)
+            return 0.0f;
+        return ev;
+    };
+    e0 = fix(x0, lo_f32(e));
+    e1 = fix(x1, hi_f32(e));
 }
 
 // Round eight fp32 values to bf16 (nearest even), two per conversion: the
@@ -157,10 +174,15 @@ swiglu_quantize_kernel(const uint4 *__restrict__ gu, int64_t M, int64_t I, uint8
         unpack8(__ldg(gu + row * in_row + c), g);
         unpack8(__ldg(gu + row * in_row + out_row + c), u);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
+        for (int e = 0; e < 8; e += 2) {
             // 1 / (1 + e^-g): the correctly rounded reciprocal is the IEEE quotient
-            const float sig = __frcp_rn(__fadd_rn(1.0f, exp_f32(-g[e])));
-            t[e] = __fmul_rn(__fmul_rn(g[e], sig), u[e]);
+            float x0, x1;
+            exp_f32x2(-g[e], -g[e + 1], x0, x1);
+            const float s0 = __frcp_rn(__fadd_rn(1.0f, x0)), s1 = __frcp_rn(__fadd_rn(1.0f, x1));
+            const uint64_t gs = ptx::mul_f32x2(ptx::pack_f32x2(g[e], g[e + 1]), ptx::pack_f32x2(s0, s1));
+            const uint64_t tu = ptx::mul_f32x2(gs, ptx::pack_f32x2(u[e], u[e + 1]));
+            t[e] = ptx::lo_f32(tu);
+            t[e + 1] = ptx::hi_f32(tu);
         }
         uint32_t w[4];
         round_bf16x8(t, w, v);

@@ -451,6 +451,14 @@ __device__ __forceinline__ void fma_f32x2(uint64_t &acc, uint64_t p, uint64_t w)
     asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(p), "l"(w));
 }
 
+// a * b + c, lane-wise (each lane one correctly rounded fused multiply-add)
+__device__ __forceinline__ uint64_t fma2_f32x2(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+
 __device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b)
 {
     uint64_t r;

@@ -140,9 +140,16 @@ rmsnorm_quantize_kernel(const uint4 *__restrict__ x, const uint4 *__restrict__ g
         float f[8], g[8], u[8], v[8];
         unpack8(__ldg(xr + c), f);
         unpack8(__ldg(gamma + c), g);
+        // (x * rstd) * gamma, two values per packed multiply (each lane
+        // rounded as the scalar multiply)
+        const uint64_t r2 = ptx::pack_f32x2(rstd, rstd);
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-            u[e] = __fmul_rn(__fmul_rn(f[e], rstd), g[e]);
+        for (int e = 0; e < 8; e += 2) {
+            const uint64_t xr2 = ptx::mul_f32x2(ptx::pack_f32x2(f[e], f[e + 1]), r2);
+            const uint64_t y2 = ptx::mul_f32x2(xr2, ptx::pack_f32x2(g[e], g[e + 1]));
+            u[e] = ptx::lo_f32(y2);
+            u[e + 1] = ptx::hi_f32(y2);
+        }
         uint32_t w[4];
         round_bf16x8(u, w, v);
         if (y)

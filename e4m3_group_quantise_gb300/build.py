@@ -1,6 +1,6 @@
 """Build the CUDA library ``libjetfp8.so`` in-tree with nvcc (sm_103a only).
 
-Three translation units (C-ABI, quantisers, GEMM) compile in parallel and
+Four translation units (C-ABI, quantisers, GEMM, producers) compile in parallel and
 link into one shared object with the CUDA runtime linked statically, so the
 library needs nothing at load time but the driver (which it reaches through
 the runtime only when a call is made).

@@ -325,11 +325,11 @@ int64_t jo_e4m3_encode_check_range(uint32_t lo, uint64_t count, const uint8_t *c
 /*                                                                    */
 /* The pages (technical summaries, "Implémentation") name fused      */
 /* activation / RMSNorm kernels that emit the FP8 input of the next  */
-/* GEMM, without their                                                */
-/* arithmetic.  The definitions below are this build's: every step is */
-/* one IEEE fp32 operation (+, *, /, sqrt, fmaf, rint) in the stated  */
-/* order, so that the CUDA kernels can reproduce them bit for bit; the */
-/* bf16 result is then quantised exactly like jo_quantize_act.        */
+/* GEMM, without their arithmetic.  The definitions below are this   */
+/* library's: every step is one IEEE fp32 operation (+, *, /, sqrt,   */
+/* fmaf, rint) in the stated order, so that the CUDA kernels can      */
+/* reproduce them bit for bit; the bf16 result is then quantised      */
+/* exactly like jo_quantize_act.                                      */
 /* ------------------------------------------------------------------ */
 
 /* fp32 -> bf16, round to nearest, ties to even (NaN kept quiet). */

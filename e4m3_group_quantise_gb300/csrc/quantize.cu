@@ -186,7 +186,7 @@ quantize_act_t_kernel(const uint4 *__restrict__ x, int64_t M, int64_t C, uint8_t
 // 128x128 weight blocks.  One CTA per block: 16 lanes cover a 128-wide row,
 // 16 rows per pass, 8 passes; amax through warp shuffles and a shared-memory
 // combine of the 8 warps.  With `qt` the codes are also staged in shared
-// memory and written transposed (each thread: 64 codes of one output row).
+// memory and written transposed (each thread: 16 codes of four output rows).
 // ---------------------------------------------------------------------------
 constexpr int Q3_THREADS = 256;
 
@@ -255,20 +255,28 @@ quantize_weight_kernel(const uint4 *__restrict__ w, int64_t N, int64_t K, uint2 
     if (qt == nullptr)
         return;
     __syncthreads();
-    // transposed write: output row kk (a column of the block), 64 codes
-    const int kk = t >> 1, hn = t & 1;
-    uint32_t o[16];
+    // transposed write: lane l of warp w takes output rows 4l .. 4l+3 (columns
+    // of the block) and their codes for block rows 16w .. 16w+15: sixteen
+    // 4-byte reads (one block row each, conflict-free across the warp), a
+    // 4 x 4 byte transpose per four rows, one 16-byte store per output row
+    const int kq = 4 * lane, n0 = 16 * warp;
+    uint32_t rw[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        const int n = 64 * hn + 4 * i;
-        o[i] = static_cast<uint32_t>(s_codes[n][kk]) | (static_cast<uint32_t>(s_codes[n + 1][kk]) << 8) |
-               (static_cast<uint32_t>(s_codes[n + 2][kk]) << 16) |
-               (static_cast<uint32_t>(s_codes[n + 3][kk]) << 24);
+    for (int i = 0; i < 16; ++i)
+        rw[i] = *reinterpret_cast<const uint32_t *>(&s_codes[n0 + i][kq]);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint32_t o[4];
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            // byte j of block rows 4b .. 4b+3: the codes of column kq + j
+            const uint32_t lo = __byte_perm(rw[4 * b], rw[4 * b + 1], j | ((4 + j) << 4));
+            const uint32_t hi = __byte_perm(rw[4 * b + 2], rw[4 * b + 3], j | ((4 + j) << 4));
+            o[b] = __byte_perm(lo, hi, 0x5410);
+        }
+        __stcs(reinterpret_cast<uint4 *>(qt + (bk * 128 + kq + j) * N + bn * 128 + n0),
+               make_uint4(o[0], o[1], o[2], o[3]));
     }
-    uint4 *dst = reinterpret_cast<uint4 *>(qt + (bk * 128 + kk) * N + bn * 128 + 64 * hn);
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-        __stcs(dst + i, make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]));
 }
 
 // ---------------------------------------------------------------------------

@@ -45,6 +45,35 @@ WORKLOAD = ("train-8b: full FP8 training step (quantise W; quantise X and X^T, d
 FP8_PER_BF16 = 4.5 / 2.25          # nominal dense fp8 : bf16 tensor ratio
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNELS = ("quant_w", "quant_x_dual", "quant_dy_dual", "fprop", "dgrad", "wgrad")
+# DRAM traffic of the dominant kernel (gemm_kernel<256,4,0,0>: the Fprop and Dgrad
+# launches), from one ncu capture of this step (dram__bytes_read.sum +
+# dram__bytes_write.sum per launch, averaged over the step's four Fprop and four Dgrad
+# launches, caches left warm as in the step; profiles/train8b_gemm_traffic.md).  It
+# describes the GEMM sources whose SHA-256 is recorded here and is reported as null
+# once they differ.
+GEMM_TRAFFIC = {"bytes_per_launch": 956.1e6,
+                "sources": ("gemm.cu", "ptx.cuh", "internal.cuh"),
+                "sha256": "cf748373eb5179dc5b6f9000424a793b4d1bb125d6877e8fbb2fc948edbd459f"}
+
+
+def gemm_sources_sha256() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "e4m3_group_quantise_gb300", "csrc")
+    for name in GEMM_TRAFFIC["sources"]:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def gemm_algorithmic_bytes(kind: str, n: int, k: int) -> float:
+    """Algorithmic bytes of one GEMM launch: both code operands, both scale sets, the bf16 output."""
+    m = TOKENS
+    if kind == "fprop":        # X [M,K], W [N,K] -> Y [M,N]
+        return m * k + n * k + 4 * (m * k // 128 + n * k // 16384) + 2 * m * n
+    if kind == "dgrad":        # dY [M,N], W^T [K,N] -> dX [M,K]
+        return m * n + n * k + 4 * (m * n // 128 + n * k // 16384) + 2 * m * k
+    return n * m + k * m + 4 * (m // 128) * (n + k) + 2 * n * k   # wgrad: dY^T, X^T -> dW [N,K]
 
 
 def gemm_flops() -> float:
@@ -423,6 +452,12 @@ def main(argv=None):
         kernels[kind] = entry
     gemm_ms = sum(kernels[k]["ms_per_step"] for k in ("fprop", "dgrad", "wgrad"))
     gemm_achieved = flops / (gemm_ms * 1e-3) / 1e12
+    # the dominant kernel: gemm_kernel<256,4,0,0>, which runs the Fprop and Dgrad launches
+    fd_flops = sum(2 * 2.0 * TOKENS * n * k for n, k in PROJ.values())
+    fd_ms = kernels["fprop"]["ms_per_step"] + kernels["dgrad"]["ms_per_step"]
+    fd_achieved = fd_flops / (fd_ms * 1e-3) / 1e12
+    fd_alg_bytes = sum(gemm_algorithmic_bytes(kd, n, k) for kd in ("fprop", "dgrad") for n, k in PROJ.values()) / 8
+    traffic_current = gemm_sources_sha256() == GEMM_TRAFFIC["sha256"]
     launches = args.steps * sum(len(r) for r in per.values()) // serial_steps
 
     result = {
@@ -434,11 +469,20 @@ def main(argv=None):
                    "projections": {k: list(v) for k, v in PROJ.items()},
                    "l2": "inputs larger than L2 (per-step working set ~8 GB vs 129 MB L2); no flush"},
         "pct_of_fp8_peak": round(100.0 * value / world / fp8_sustained, 1),
-        "roofline": {"kernel": "gemm (fprop+dgrad+wgrad launches, serial pass)", "bound": "tensor",
-                     "achieved": round(gemm_achieved, 1), "peak": round(fp8_sustained, 1), "unit": "TFLOP/s",
-                     "frac": round(gemm_achieved / fp8_sustained, 3), "traffic": None,
+        "roofline": {"kernel": "gemm_kernel<256,4,0,0>: the 4 Fprop + 4 Dgrad launches of a step, serial pass",
+                     "bound": "tensor",
+                     "achieved": round(fd_achieved, 1), "peak": round(fp8_sustained, 1), "unit": "TFLOP/s",
+                     "frac": round(fd_achieved / fp8_sustained, 3),
+                     "traffic": GEMM_TRAFFIC["bytes_per_launch"] if traffic_current else None,
+                     "algorithmic_bytes": round(fd_alg_bytes),
+                     "traffic_note": ("DRAM bytes per launch (read + write, ncu, average of the 8 launches), "
+                                      "profiles/train8b_gemm_traffic.md" if traffic_current else
+                                      "null: the GEMM sources differ from those the traffic was captured on"),
                      "peak_note": f"{src} bf16_tflops_sustained x {FP8_PER_BF16} (nominal fp8:bf16 ratio), "
                                   f"'of {src}'"},
+        "gemm_all": {"kernels": "every GEMM launch of the step (Fprop, Dgrad, Wgrad), serial pass",
+                     "achieved": round(gemm_achieved, 1), "unit": "TFLOP/s",
+                     "frac": round(gemm_achieved / fp8_sustained, 3)},
         "kernels": kernels,
         "kernels_timing": f"each launch between CUDA events on its stream, in a serial pass of {serial_steps} "
                           "steps right after the timed region (the timed region overlaps dY quantisation and "

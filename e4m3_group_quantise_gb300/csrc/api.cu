@@ -232,7 +232,11 @@ JETFP8_API jetfp8_status jetfp8_quantize_act_dual(const void *x, int64_t M, int6
     jetfp8_status status = current_device(&dev);
     if (status != JETFP8_OK)
         return status;
-    return launch_status(jetfp8::launch_quantize_act_dual(x, M, K, q, s, qt, st, static_cast<cudaStream_t>(stream)));
+    std::call_once(g_encode_once, init_encode);
+    if (g_encode == nullptr)
+        return JETFP8_ERR_UNSUPPORTED_DEVICE;
+    return launch_status(jetfp8::launch_quantize_act_dual(x, M, K, q, s, qt, st, g_encode, dev->err_word,
+                                                          static_cast<cudaStream_t>(stream)));
 }
 
 JETFP8_API jetfp8_status jetfp8_quantize_weight(const void *w, int64_t N, int64_t K, uint8_t *q, float *s,

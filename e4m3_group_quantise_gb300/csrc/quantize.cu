@@ -284,29 +284,43 @@ quantize_weight_kernel(const uint4 *__restrict__ w, int64_t N, int64_t K, uint2 
 // scales (as quantize_act_kernel) and the 128x1 column-group codes and scales
 // written transposed (as quantize_act_t_kernel).  One CTA (8 warps) per 128 x
 // 128 tile:
-//   rows:    warp w loads rows 16w .. 16w+15 straight from global memory,
-//            eight rows per step, four lanes per row holding 32 values each
-//            (16-byte chunks sub, sub + 4, sub + 8, sub + 12), and encodes them
-//            as it goes: one scale per 32 values per lane, amax in two
-//            shuffles, codes in 32-byte runs.  The raw values also go to a
-//            shared tile, 16-byte chunks XOR-swizzled by (row & 15).
-//   columns: after one block barrier, warp w takes 8-column chunk w (then
-//            w + 8) and reads it with four transposing matrix loads
-//            (ldmatrix .trans, 32 rows each, conflict-free thanks to the
-//            swizzle): lane 4c + q then holds column c, rows 8j + 2q and
-//            8j + 2q + 1 for j = 0..15, so a 128x1 group is four lanes of one
-//            warp (amax: two shuffles).  The interleaved codes are put back in
-//            row order through a small per-warp staging buffer and leave as
-//            two 16-byte stores per lane.
+//   load:    two bulk tensor copies (tensor memory accelerator) bring the tile
+//            into shared memory as two 64-column halves with the 128-byte
+//            swizzle (16-byte chunk c of row r at position c ^ (r & 7)); every
+//            thread waits on one mbarrier, bounded, and the block gives up
+//            together if the copies never land.
+//   rows:    warp w takes rows 16w .. 16w+15, eight rows per step, four lanes
+//            per row holding 32 values each (16-byte chunks sub, sub + 4,
+//            sub + 8, sub + 12), and encodes them: one scale per 32 values per
+//            lane, amax in two shuffles, codes in 32-byte runs.
+//   columns: warp w then takes 8-column chunk w (then w + 8) and reads it with
+//            four transposing matrix loads (ldmatrix .trans, 32 rows each,
+//            conflict-free thanks to the swizzle): lane 4c + q then holds
+//            column c, rows 8j + 2q and 8j + 2q + 1 for j = 0..15, so a 128x1
+//            group is four lanes of one warp (amax: two shuffles).  The tile is
+//            read-only once it has landed, so no barrier separates the passes.
+//            The interleaved codes are put back in row order through a small
+//            per-warp staging buffer and leave as two 16-byte stores per lane.
 // ---------------------------------------------------------------------------
 constexpr int QD_TILE = 128;
 constexpr int QD_THREADS = 256;
 constexpr int QD_STAGE_PITCH = 140;          // bytes per staged column (35 words: writes and reads bank-conflict free)
 
 struct DualSmem {
-    uint4 tile[QD_TILE][QD_TILE / 8];                          // 32 KB
+    // the 128 x 128 bf16 tile as two 64-column halves written by the tensor
+    // memory accelerator with its 128-byte swizzle: 16-byte chunk c of row r
+    // of a half sits at position c ^ (r & 7) of the row (1024-byte aligned)
+    uint8_t tile[2][QD_TILE][128];                             // 32 KB
     uint8_t stage[QD_THREADS / 32][8][QD_STAGE_PITCH];        // codes of 8 columns per warp
+    uint64_t bar;
 };
+constexpr uint32_t QD_SMEM_BYTES = sizeof(DualSmem) + 1024;    // + alignment slack
+
+// Address of 16-byte chunk c (0..15) of tile row r.
+__device__ __forceinline__ const uint8_t *dual_chunk(const DualSmem &sm, int r, int c)
+{
+    return &sm.tile[c >> 3][r][((c & 7) ^ (r & 7)) << 4];
+}
 
 __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], const void *row_addr)
 {
@@ -317,16 +331,34 @@ __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], const void *
 }
 
 __global__ void __launch_bounds__(QD_THREADS)
-quantize_act_dual_kernel(const uint4 *__restrict__ x, int64_t M, int64_t K, uint8_t *__restrict__ q,
-                         float *__restrict__ s, uint8_t *__restrict__ qt, float *__restrict__ st)
+quantize_act_dual_kernel(const __grid_constant__ CUtensorMap tmap_x, int64_t M, int64_t K, uint8_t *__restrict__ q,
+                         float *__restrict__ s, uint8_t *__restrict__ qt, float *__restrict__ st,
+                         uint32_t *__restrict__ err)
 {
-    extern __shared__ __align__(16) uint8_t dual_smem_raw[];
-    DualSmem &sm = *reinterpret_cast<DualSmem *>(dual_smem_raw);
+    extern __shared__ uint8_t dual_smem_raw[];
+    DualSmem &sm = *reinterpret_cast<DualSmem *>((reinterpret_cast<uintptr_t>(dual_smem_raw) + 1023) &
+                                                 ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t K8 = K >> 3;
     const int64_t tiles_k = K / QD_TILE;
     const int64_t m0 = (static_cast<int64_t>(blockIdx.x) / tiles_k) * QD_TILE;
     const int64_t k0 = (static_cast<int64_t>(blockIdx.x) % tiles_k) * QD_TILE;
+
+    // the whole tile arrives by two bulk tensor copies; every thread waits
+    // (bounded) for them, and the block gives up together if they never land
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(&sm.bar, 1);
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        ptx::mbar_arrive_expect_tx(&sm.bar, 2 * QD_TILE * 128);
+        ptx::tma_load_2d(&sm.tile[0][0][0], &tmap_x, &sm.bar, static_cast<int32_t>(k0), static_cast<int32_t>(m0));
+        ptx::tma_load_2d(&sm.tile[1][0][0], &tmap_x, &sm.bar, static_cast<int32_t>(k0 + 64),
+                         static_cast<int32_t>(m0));
+    }
+    const bool landed = ptx::mbar_wait(&sm.bar, 0, nullptr, err, ERRBIT_QUANT, 2000000000ull);
+    if (__syncthreads_or(!landed))
+        return;
 
     // ---- rows: 16 per warp, 8 per step; four lanes per row, 32 values each
     //      (16-byte chunks sub, sub+4, sub+8, sub+12 of the row's 256 bytes)
@@ -335,17 +367,14 @@ quantize_act_dual_kernel(const uint4 *__restrict__ x, int64_t M, int64_t K, uint
 #pragma unroll
         for (int step = 0; step < 2; ++step) {
             const int r = 16 * warp + 8 * step + rr;
-            const uint4 *src = x + (m0 + r) * K8 + (k0 >> 3);
             uint4 v[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-                v[j] = __ldg(src + sub + 4 * j);
+                v[j] = *reinterpret_cast<const uint4 *>(dual_chunk(sm, r, sub + 4 * j));
             float f[32];
             float amax = 0.0f;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const int c = sub + 4 * j;
-                sm.tile[r][c ^ (r & 15)] = v[j];
                 float u[8];
                 unpack8(v[j], u);
 #pragma unroll
@@ -372,14 +401,13 @@ quantize_act_dual_kernel(const uint4 *__restrict__ x, int64_t M, int64_t K, uint
                 const int k = __ffs(redo) - 1;
                 redo &= redo - 1u;
                 const int c = sub + 4 * (k >> 1);
-                const uint2 in = reinterpret_cast<const uint2 *>(&sm.tile[r][c ^ (r & 15)])[k & 1];
+                const uint2 in = reinterpret_cast<const uint2 *>(dual_chunk(sm, r, c))[k & 1];
                 *reinterpret_cast<uint32_t *>(row_q + 8 * c + 4 * (k & 1)) = encode4_exact(in, gs.s);
             }
         }
     }
-    __syncthreads();
-
-    // ---- columns: chunk w, then w + 8 -------------------------------------
+    // ---- columns: chunk w, then w + 8 (the tile is read-only from here on:
+    //      no barrier between the passes) -----------------------------------
     const int cq = lane & 3;                         // q: which row pairs of each 8-row block
     const int cc = lane >> 2;                        // column within the 8-column chunk
     uint8_t *stg = &sm.stage[warp][0][0];
@@ -391,7 +419,7 @@ quantize_act_dual_kernel(const uint4 *__restrict__ x, int64_t M, int64_t K, uint
         for (int j = 0; j < 4; ++j) {
             const int r = 32 * j + lane;              // this lane's row address for the x4 load
             uint32_t t4[4];
-            ldmatrix_x4_trans(t4, &sm.tile[r][chunk ^ (r & 15)]);
+            ldmatrix_x4_trans(t4, dual_chunk(sm, r, chunk));
 #pragma unroll
             for (int m = 0; m < 4; ++m)
                 wv[4 * j + m] = t4[m];               // rows 8(4j+m) + 2cq, +1 of column cc
@@ -430,7 +458,7 @@ quantize_act_dual_kernel(const uint4 *__restrict__ x, int64_t M, int64_t K, uint
                 for (int e = 0; e < 4; ++e) {
                     const int rr = 16 * k + 8 * (e >> 1) + 2 * cq + (e & 1);
                     const uint16_t h =
-                        reinterpret_cast<const uint16_t *>(&sm.tile[rr][chunk ^ (rr & 15)])[colw & 7];
+                        reinterpret_cast<const uint16_t *>(dual_chunk(sm, rr, chunk))[colw & 7];
                     v4[e] = __uint_as_float(static_cast<uint32_t>(h) << 16);
                 }
                 const uint32_t fixed = encode4_exact(v4[0], v4[1], v4[2], v4[3], gs.s);
@@ -485,15 +513,26 @@ cudaError_t launch_quantize_weight(const void *w, int64_t N, int64_t K, uint8_t 
 
 namespace jetfp8 {
 cudaError_t launch_quantize_act_dual(const void *x, int64_t M, int64_t K, uint8_t *q, float *s, uint8_t *qt,
-                                     float *st, cudaStream_t stream)
+                                     float *st, PFN_cuTensorMapEncodeTiled_v12000 encode, uint32_t *err,
+                                     cudaStream_t stream)
 {
+    // X [M][K] bf16 seen as 128-row x 64-column boxes with the 128-byte swizzle
+    CUtensorMap tmap;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(QD_TILE)};
+    cuuint32_t estr[2] = {1, 1};
+    if (encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(x), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(quantize_act_dual_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(sizeof(DualSmem)));
+                                         static_cast<int>(QD_SMEM_BYTES));
     if (e != cudaSuccess)
         return e;
     const int64_t tiles = (M / QD_TILE) * (K / QD_TILE);
-    quantize_act_dual_kernel<<<static_cast<unsigned>(tiles), QD_THREADS, sizeof(DualSmem), stream>>>(
-        static_cast<const uint4 *>(x), M, K, q, s, qt, st);
+    quantize_act_dual_kernel<<<static_cast<unsigned>(tiles), QD_THREADS, QD_SMEM_BYTES, stream>>>(tmap, M, K, q, s,
+                                                                                                  qt, st, err);
     return cudaGetLastError();
 }
 }  // namespace jetfp8

@@ -49,11 +49,11 @@ KERNELS = ("quant_w", "quant_x_dual", "quant_dy_dual", "fprop", "dgrad", "wgrad"
 # launches), from one ncu capture of this step (dram__bytes_read.sum +
 # dram__bytes_write.sum per launch, averaged over the step's four Fprop and four Dgrad
 # launches, caches left warm as in the step; profiles/train8b_gemm_traffic.md).  It
-# describes the GEMM sources whose SHA-256 is recorded here and is reported as null
-# once they differ.
+# describes the kernel built from the sources whose SHA-256 is recorded here (the
+# kernel and its inline-PTX helpers) and is reported as null once they differ.
 GEMM_TRAFFIC = {"bytes_per_launch": 956.1e6,
-                "sources": ("gemm.cu", "ptx.cuh", "internal.cuh"),
-                "sha256": "cf748373eb5179dc5b6f9000424a793b4d1bb125d6877e8fbb2fc948edbd459f"}
+                "sources": ("gemm.cu", "ptx.cuh"),
+                "sha256": "c260b711ab27533bc53a3f27d633ea8fa719ca5fbd05ea7f69e3974460bebb82"}
 
 
 def gemm_sources_sha256() -> str:

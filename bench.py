@@ -66,6 +66,16 @@ def gemm_sources_sha256() -> str:
     return h.hexdigest()
 
 
+def gemm_traffic():
+    """(DRAM bytes per launch of the dominant kernel, note); (None, reason) once
+    the kernel's sources differ from those the bytes were captured on."""
+    if gemm_sources_sha256() == GEMM_TRAFFIC["sha256"]:
+        return (GEMM_TRAFFIC["bytes_per_launch"],
+                "DRAM bytes per launch (read + write, ncu, average of the 8 launches), "
+                "profiles/train8b_gemm_traffic.md")
+    return None, "null: the GEMM sources differ from those the traffic was captured on"
+
+
 def gemm_algorithmic_bytes(kind: str, n: int, k: int) -> float:
     """Algorithmic bytes of one GEMM launch: both code operands, both scale sets, the bf16 output."""
     m = TOKENS
@@ -457,7 +467,7 @@ def main(argv=None):
     fd_ms = kernels["fprop"]["ms_per_step"] + kernels["dgrad"]["ms_per_step"]
     fd_achieved = fd_flops / (fd_ms * 1e-3) / 1e12
     fd_alg_bytes = sum(gemm_algorithmic_bytes(kd, n, k) for kd in ("fprop", "dgrad") for n, k in PROJ.values()) / 8
-    traffic_current = gemm_sources_sha256() == GEMM_TRAFFIC["sha256"]
+    traffic, traffic_note = gemm_traffic()
     launches = args.steps * sum(len(r) for r in per.values()) // serial_steps
 
     result = {
@@ -473,11 +483,9 @@ def main(argv=None):
                      "bound": "tensor",
                      "achieved": round(fd_achieved, 1), "peak": round(fp8_sustained, 1), "unit": "TFLOP/s",
                      "frac": round(fd_achieved / fp8_sustained, 3),
-                     "traffic": GEMM_TRAFFIC["bytes_per_launch"] if traffic_current else None,
+                     "traffic": traffic,
                      "algorithmic_bytes": round(fd_alg_bytes),
-                     "traffic_note": ("DRAM bytes per launch (read + write, ncu, average of the 8 launches), "
-                                      "profiles/train8b_gemm_traffic.md" if traffic_current else
-                                      "null: the GEMM sources differ from those the traffic was captured on"),
+                     "traffic_note": traffic_note,
                      "peak_note": f"{src} bf16_tflops_sustained x {FP8_PER_BF16} (nominal fp8:bf16 ratio), "
                                   f"'of {src}'"},
         "gemm_all": {"kernels": "every GEMM launch of the step (Fprop, Dgrad, Wgrad), serial pass",

@@ -8,6 +8,7 @@ from .jetfp8 import (  # noqa: F401
     gemm_fprop,
     gemm_wgrad,
     jetfp8_act_scale_count,
+    jetfp8_e4m3_encode_range,
     jetfp8_gemm_dgrad,
     jetfp8_gemm_fprop,
     jetfp8_gemm_wgrad,

@@ -239,6 +239,24 @@ JETFP8_API jetfp8_status jetfp8_quantize_act_dual(const void *x, int64_t M, int6
                                                           static_cast<cudaStream_t>(stream)));
 }
 
+JETFP8_API jetfp8_status jetfp8_e4m3_encode_range(uint32_t first, int64_t count, uint8_t *codes, void *stream)
+{
+    if (count < 0 || count > (int64_t{1} << 32) - static_cast<int64_t>(first))
+        return JETFP8_ERR_SHAPE;
+    if (count == 0)
+        return JETFP8_OK;
+    if (!codes)
+        return JETFP8_ERR_INVALID_VALUE;
+    if (!aligned16(codes))
+        return JETFP8_ERR_ALIGNMENT;
+    const DeviceInfo *dev = nullptr;
+    jetfp8_status status = current_device(&dev);
+    if (status != JETFP8_OK)
+        return status;
+    return launch_status(
+        jetfp8::launch_e4m3_encode_range(first, count, codes, dev->sm_count, static_cast<cudaStream_t>(stream)));
+}
+
 JETFP8_API jetfp8_status jetfp8_quantize_weight(const void *w, int64_t N, int64_t K, uint8_t *q, float *s,
                                                 uint8_t *qt, void *stream)
 {

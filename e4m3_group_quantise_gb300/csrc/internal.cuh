@@ -30,6 +30,8 @@ cudaError_t launch_quantize_act_dual(const void *x, int64_t M, int64_t K, uint8_
                                      cudaStream_t stream);
 cudaError_t launch_quantize_weight(const void *w, int64_t N, int64_t K, uint8_t *q, float *s, uint8_t *qt,
                                    cudaStream_t stream);
+cudaError_t launch_e4m3_encode_range(uint32_t first, int64_t count, uint8_t *codes, int sm_count,
+                                     cudaStream_t stream);
 
 // Fused producers (producers.cu): RMSNorm / SwiGLU -> bf16 -> 1x128 FP8.
 // q and s may be null (then only y is written); y may be null.

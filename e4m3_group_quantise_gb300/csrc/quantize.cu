@@ -509,6 +509,46 @@ cudaError_t launch_quantize_weight(const void *w, int64_t N, int64_t K, uint8_t 
     return cudaGetLastError();
 }
 
+namespace {
+// codes[i] = E4M3 code of the fp32 pattern first + i, through the same
+// conversion instruction the quantisers use; eight patterns per thread.
+__global__ void __launch_bounds__(256) e4m3_encode_range_kernel(uint32_t first, int64_t count,
+                                                                 uint8_t *__restrict__ codes)
+{
+    const int64_t words = (count + 7) >> 3;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < words;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t base = 8 * i;
+        uint32_t w[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            float v[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)   // patterns past the end wrap around; they are not stored
+                v[e] = __uint_as_float(first + static_cast<uint32_t>(base + 4 * h + e));
+            w[h] = ptx::cvt_e4m3x2(v[0], v[1]) | (ptx::cvt_e4m3x2(v[2], v[3]) << 16);
+        }
+        if (base + 8 <= count) {
+            *reinterpret_cast<uint2 *>(codes + base) = make_uint2(w[0], w[1]);
+        } else {
+            for (int e = 0; base + e < count; ++e)
+                codes[base + e] = static_cast<uint8_t>(w[e >> 2] >> (8 * (e & 3)));
+        }
+    }
+}
+}  // namespace
+
+cudaError_t launch_e4m3_encode_range(uint32_t first, int64_t count, uint8_t *codes, int sm_count,
+                                     cudaStream_t stream)
+{
+    const int64_t words = (count + 7) / 8;
+    const int64_t want = (words + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(sm_count) * 8;
+    e4m3_encode_range_kernel<<<static_cast<unsigned>(want < cap ? want : cap), 256, 0, stream>>>(first, count,
+                                                                                                 codes);
+    return cudaGetLastError();
+}
+
 }  // namespace jetfp8
 
 namespace jetfp8 {

@@ -68,6 +68,8 @@ def load_library():
                  "jetfp8_quantize_act_dual", "jetfp8_rmsnorm_quantize_act", "jetfp8_swiglu_quantize_act",
                  "jetfp8_gemm_fprop", "jetfp8_gemm_dgrad", "jetfp8_gemm_wgrad"):
         getattr(lib, name).restype = S
+    lib.jetfp8_e4m3_encode_range.argtypes = [ctypes.c_uint32, I, P, P]
+    lib.jetfp8_e4m3_encode_range.restype = S
     lib.jetfp8_act_scale_count.argtypes = [I, I]
     lib.jetfp8_act_scale_count.restype = ctypes.c_size_t
     lib.jetfp8_status_string.argtypes = [S]
@@ -186,6 +188,14 @@ def jetfp8_quantize_weight(w, q, s, qt=None, stream=None):
         _want(qt, torch.uint8, (K, N), "qt")
     _check(load_library().jetfp8_quantize_weight(_ptr(w), N, K, _ptr(q), _ptr(s), _ptr(qt), _stream(stream)),
            "jetfp8_quantize_weight")
+
+
+def jetfp8_e4m3_encode_range(first, codes, stream=None):
+    """codes[i] = the GPU's E4M3 code of the fp32 pattern first + i (a test hook
+    for the conversion the quantisers end in)."""
+    _want(codes, torch.uint8, (codes.numel(),), "codes")
+    _check(load_library().jetfp8_e4m3_encode_range(int(first), codes.numel(), _ptr(codes), _stream(stream)),
+           "jetfp8_e4m3_encode_range")
 
 
 def jetfp8_gemm_fprop(qx, sx, qw, sw, y, stream=None):

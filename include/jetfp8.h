@@ -217,6 +217,18 @@ JETFP8_API jetfp8_status jetfp8_gemm_wgrad(const uint8_t *qdyt, const float *sdy
                                            void *dw, int64_t M, int64_t N, int64_t K,
                                            void *stream);
 
+/*
+ * Test hook for the conversion every quantiser ends in: codes[i] = the
+ * OCP E4M3 code (round to nearest even, saturating to +-448, NaN -> 0x7F or
+ * 0xFF by sign) that the GPU's E4M3 conversion gives for the fp32 value whose
+ * bit pattern is first + i, i = 0 .. count-1.  Lets a test compare the
+ * hardware conversion with a reference over all 2^32 fp32 patterns, in
+ * chunks.
+ *   codes : uint8 [count], device memory, 16-byte aligned (output)
+ * Requires 0 <= count <= 2^32 - first.
+ */
+JETFP8_API jetfp8_status jetfp8_e4m3_encode_range(uint32_t first, int64_t count, uint8_t *codes, void *stream);
+
 /* Number of fp32 scales of a [rows][cols] tensor quantised in 1x128 groups
  * along cols: (cols / 128) * rows.  Returns 0 for invalid sizes. */
 JETFP8_API size_t jetfp8_act_scale_count(int64_t rows, int64_t cols);

@@ -49,6 +49,16 @@ D16 = 0x60000000
 E16 = 0x80000000
 
 
+def test_e4m3_encode_range_validation(lib):
+    f = lib.jetfp8_e4m3_encode_range
+    assert f(0, -1, B16, None) == J.ERR_SHAPE
+    assert f(0, (1 << 32) + 1, B16, None) == J.ERR_SHAPE         # past the last pattern
+    assert f(0xFFFFFFFF, 2, B16, None) == J.ERR_SHAPE
+    assert f(7, 0, None, None) == J.OK                            # empty: nothing to do
+    assert f(0, 16, None, None) == J.ERR_INVALID_VALUE
+    assert f(0, 16, B16 + 8, None) == J.ERR_ALIGNMENT
+
+
 def test_quantize_act_validation(lib):
     f = lib.jetfp8_quantize_act
     assert f(A16, 4, 100, B16, C16, None) == J.ERR_SHAPE          # K % 128

@@ -86,7 +86,6 @@ struct KernelArgs {
     uint32_t *err;
     int32_t rows, cols, groups;
     int32_t tiles_m, tiles_n;
-    int32_t tiles_nw;     // work-item columns: tiles_n, or tile pairs (ceil(tiles_n / 2)) for CTA pairs
 };
 
 template <int BN, int STAGES>
@@ -132,14 +131,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 __device__ __forceinline__ void tmem_ld_quads(uint32_t taddr, uint32_t (&r)[32]) { ptx::tmem_ld_16x256b_x8(taddr, r); }
 __device__ __forceinline__ void tmem_ld_quads(uint32_t taddr, uint32_t (&r)[16]) { ptx::tmem_ld_16x256b_x4(taddr, r); }
 
-// PAIR: the kernel runs as clusters of two CTAs that compute horizontally
-// adjacent 128 x BN tiles (same rows).  Each CTA loads half of the shared A
-// tile and multicasts it to both; a stage is refilled only after both CTAs'
-// MMAs have released it (each MMA issuer's commit arrives on both CTAs' empty
-// barriers).  With BN = 128 this halves each SM's accumulator tile, so TMEM
-// holds four partial buffers (the release chain then overlaps three groups of
-// MMAs) while the L2 traffic per FLOP stays that of a 128 x 256 tile.
-template <int BN, int STAGES, bool SB_PER_COLUMN, bool PAIR>
+template <int BN, int STAGES, bool SB_PER_COLUMN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
             const __grid_constant__ CUtensorMap tmap_d, const KernelArgs args)
@@ -165,24 +157,21 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     constexpr int PS = 4;                        // blocks per slab
     constexpr int NPS = CB / PS;                 // slabs per group
     static_assert(CB % PS == 0, "32-column slabs");
-    // TMEM partial buffers: two 256-wide ones; four 128-wide ones (also for
-    // CTA pairs); eight for narrower (decode) tiles, so that the MMAs can run
-    // several groups ahead of the read-back instead of waiting on every
-    // hand-off.
-    constexpr uint32_t NBUF = PAIR ? 4 : (BN >= 256 ? 2 : (BN == 128 ? 4 : MAX_TBUF));
+    // TMEM partial buffers: two 256-wide ones; four 128-wide ones; eight for
+    // narrower (decode) tiles, so that the MMAs can run several groups ahead
+    // of the read-back instead of waiting on every hand-off.
+    constexpr uint32_t NBUF = BN >= 256 ? 2 : (BN == 128 ? 4 : MAX_TBUF);
     // The MMA issuers commit only the TMEM-full barrier: its completion also
     // means the group's MMAs have read their shared-memory stage, and the
     // first promotion warp, seeing it, releases the stage to the producer.
     // One commit per group shortens the issue loop, which sits in the chain
     // of hand-offs (measured: decode tiles 5-9 % faster, 256-wide tiles about
-    // even).  CTA pairs keep the multicast commit to both CTAs' stages.
-    constexpr bool PROMO_RELEASES_STAGE = !PAIR;
+    // even).
     // A second MMA issuer (the otherwise idle fourth control warp): even
     // groups from the MMA warp, odd groups from warp 3, into different TMEM
     // buffers, so one group's MMAs are issued as soon as its buffer is free
     // rather than after the previous group's issue loop (the issue of a
     // group's four MMAs and commits takes a few hundred cycles).
-    constexpr bool TWO_ISSUERS = !PAIR;
     constexpr int SECOND_MMA_WARP = 3;
     constexpr uint32_t TMEM_COLS = NBUF * BN;
     static_assert(TMEM_COLS <= 512, "TMEM holds 512 columns");
@@ -206,22 +195,16 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int G = args.groups;
-    // work items: tiles, or (for CTA pairs) tile pairs shared by the cluster
-    const int num_work = args.tiles_m * args.tiles_nw;
-    const int work_first = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
-    const int work_stride = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
-    const int rank = PAIR ? static_cast<int>(ptx::cluster_ctarank()) : 0;
-    auto coords = [&](int w, int &tm, int &tn) {
-        tile_coords(w, args.tiles_m, args.tiles_nw, tm, tn);
-        if (PAIR)
-            tn = 2 * tn + rank;
-    };
+    const int num_work = args.tiles_m * args.tiles_n;
+    const int work_first = static_cast<int>(blockIdx.x);
+    const int work_stride = static_cast<int>(gridDim.x);
+    auto coords = [&](int w, int &tm, int &tn) { tile_coords(w, args.tiles_m, args.tiles_n, tm, tn); };
 
     if (warp == PRODUCER_WARP) {
         if (lane == 0) {
             for (int s = 0; s < STAGES; ++s) {
                 ptx::mbar_init(&full[s], 1);
-                ptx::mbar_init(&empty[s], PAIR ? 2 : 1);   // both CTAs' MMA issuers for pairs
+                ptx::mbar_init(&empty[s], 1);   // the first promotion warp
             }
             for (int s = 0; s < SCALE_STAGES; ++s) {
                 // per-column scales: the producer's expect-tx arrival; otherwise
@@ -233,7 +216,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                 ptx::mbar_init(&tfull[b], 1);
                 ptx::mbar_init(&tempty[b], 4 * NWG);   // one arrival per promotion warp
             }
-            ptx::mbar_init(mma_done, TWO_ISSUERS ? 2 : 1);   // one final commit per MMA issuer
+            ptx::mbar_init(mma_done, 2);   // one final commit per MMA issuer
             *abort_flag = 0;
             ptx::fence_mbar_init();
             ptx::tma_prefetch_desc(&tmap_a);
@@ -246,8 +229,6 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
-    if (PAIR)
-        ptx::cluster_sync();   // the peer's barriers exist before any multicast reaches them
     const uint32_t tmem_base = *tmem_holder;
 
     if (warp < FIRST_PROMO_WARP) {
@@ -293,11 +274,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                             break;
                         }
                         ptx::mbar_arrive_expect_tx(&full[stage], L::STAGE_BYTES);
-                        if (PAIR)   // this CTA's half of the shared A tile, to both CTAs
-                            ptx::tma_load_2d_multicast(sA + stage * L::A_BYTES + rank * (L::A_BYTES / 2), &tmap_a,
-                                                       &full[stage], g * BK, tm * BM + rank * (BM / 2), 0x3);
-                        else
-                            ptx::tma_load_2d(sA + stage * L::A_BYTES, &tmap_a, &full[stage], g * BK, tm * BM);
+                        ptx::tma_load_2d(sA + stage * L::A_BYTES, &tmap_a, &full[stage], g * BK, tm * BM);
                         ptx::tma_load_2d(sB + stage * L::B_BYTES, &tmap_b, &full[stage], g * BK, tn * BN);
                         issued_mask |= 1u << stage;
                         issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -324,7 +301,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                 }
             }
             __syncwarp();
-        } else if (warp == MMA_WARP || (TWO_ISSUERS && warp == SECOND_MMA_WARP)) {
+        } else if (warp == MMA_WARP || warp == SECOND_MMA_WARP) {
             // -------------------------------------------------- MMA issuer(s)
             if (lane == 0) {
                 const uint32_t parity = warp == MMA_WARP ? 0u : 1u;   // groups this issuer takes
@@ -334,7 +311,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                 const uint32_t b_base = ptx::smem_u32(sB);
                 for (int tile = work_first; ok && tile < num_work; tile += work_stride) {
                     for (int g = 0; g < G; ++g, ++it) {
-                        if (TWO_ISSUERS && (it & 1u) != parity)
+                        if ((it & 1u) != parity)
                             continue;
                         const int stage = static_cast<int>(it % STAGES);
                         const uint32_t phase = (it / STAGES) & 1u;
@@ -354,10 +331,6 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
 #pragma unroll
                         for (int j = 0; j < BK / 32; ++j)   // 32 bytes of K per instruction: +2 in the >>4 field
                             ptx::mma_f8(d_tmem, adesc + 2 * j, bdesc + 2 * j, IDESC, j > 0 ? 1u : 0u);
-                        if (PAIR)
-                            ptx::mma_commit_multicast(&empty[stage], 0x3);
-                        else if (!PROMO_RELEASES_STAGE)
-                            ptx::mma_commit(&empty[stage]);
                         ptx::mma_commit(&tfull[buf]);
                     }
                 }
@@ -460,7 +433,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                     break;
                 }
                 ptx::tc_fence_after();
-                if (PROMO_RELEASES_STAGE && warp == FIRST_PROMO_WARP && lane == 0)
+                if (warp == FIRST_PROMO_WARP && lane == 0)
                     ptx::mbar_arrive(&empty[it % STAGES]);      // the group's MMAs are done with it
                 const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + buf * BN +
                                        wg * COLS_PER_WG;
@@ -616,17 +589,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     ptx::tc_fence_after();
     if (warp == PRODUCER_WARP)
         ptx::tmem_dealloc(tmem_base, TMEM_COLS);
-    if (PAIR)
-        ptx::cluster_sync();   // neither CTA leaves while the other may still write to it
 }
 
-template <int BN, int STAGES, bool SB_PER_COLUMN, bool PAIR>
+template <int BN, int STAGES, bool SB_PER_COLUMN>
 cudaError_t launch_variant(const GemmProblem &p, const DeviceInfo &dev, const CUtensorMap &ta, const CUtensorMap &tb,
                            const CUtensorMap &td, cudaStream_t stream)
 {
     using L = Smem<BN, STAGES>;
     static_assert(L::TOTAL <= 227 * 1024, "shared memory per CTA");
-    auto kern = gemm_kernel<BN, STAGES, SB_PER_COLUMN, PAIR>;
+    auto kern = gemm_kernel<BN, STAGES, SB_PER_COLUMN>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(L::TOTAL));
     if (e != cudaSuccess)
         return e;
@@ -642,36 +613,9 @@ cudaError_t launch_variant(const GemmProblem &p, const DeviceInfo &dev, const CU
     a.groups = static_cast<int32_t>(p.kdim / BK);
     a.tiles_m = static_cast<int32_t>((p.rows + BM - 1) / BM);
     a.tiles_n = static_cast<int32_t>((p.cols + BN - 1) / BN);
-    a.tiles_nw = PAIR ? (a.tiles_n + 1) / 2 : a.tiles_n;
-    const int work = a.tiles_m * a.tiles_nw;
-    if (!PAIR) {
-        const int grid = work < dev.sm_count ? work : dev.sm_count;
-        kern<<<grid, NUM_THREADS, L::TOTAL, stream>>>(ta, tb, td, a);
-        return cudaGetLastError();
-    }
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(NUM_THREADS);
-    cfg.dynamicSmemBytes = L::TOTAL;
-    cfg.stream = stream;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cfg.gridDim = dim3(static_cast<unsigned>(2 * work));
-    int clusters = 0;
-    e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
-    if (e != cudaSuccess)
-        return e;
-    if (clusters < 1)
-        return cudaErrorLaunchOutOfResources;
-    const int n = work < clusters ? work : clusters;
-    cfg.gridDim = dim3(static_cast<unsigned>(2 * n));
-    e = cudaLaunchKernelEx(&cfg, kern, ta, tb, td, a);
-    if (e != cudaSuccess)
-        return e;
+    const int work = a.tiles_m * a.tiles_n;
+    const int grid = work < dev.sm_count ? work : dev.sm_count;
+    kern<<<grid, NUM_THREADS, L::TOTAL, stream>>>(ta, tb, td, a);
     return cudaGetLastError();
 }
 
@@ -713,7 +657,6 @@ cudaError_t launch_gemm(const GemmProblem &p, const DeviceInfo &dev, PFN_cuTenso
     // problems get 128 x 256 tiles.  The width never changes how an output
     // element is reduced.
     const int64_t tm_count = (p.rows + BM - 1) / BM;
-    const bool pair = false;   // CTA pairs of 128 x 128 tiles: measured slower than wide tiles so far
     int bn = 256;
     int64_t best_waves = -1;
     for (int w : {256, 128, 64, 32}) {
@@ -725,27 +668,24 @@ cudaError_t launch_gemm(const GemmProblem &p, const DeviceInfo &dev, PFN_cuTenso
         }
     }
     CUtensorMap ta, tb, td;
-    if (encode_operand(encode, &ta, p.a, p.rows, p.kdim, pair ? BM / 2 : BM) != CUDA_SUCCESS ||
+    if (encode_operand(encode, &ta, p.a, p.rows, p.kdim, BM) != CUDA_SUCCESS ||
         encode_operand(encode, &tb, p.b, p.cols, p.kdim, bn) != CUDA_SUCCESS ||
         encode_output(encode, &td, p.d, p.rows, p.cols) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     const bool per_col = p.sb_mode == ScaleB::PerColumn;
-    if (pair)
-        return per_col ? launch_variant<128, 6, true, true>(p, dev, ta, tb, td, stream)
-                       : launch_variant<128, 6, false, true>(p, dev, ta, tb, td, stream);
     switch (bn) {
     case 256:
-        return per_col ? launch_variant<256, 4, true, false>(p, dev, ta, tb, td, stream)
-                       : launch_variant<256, 4, false, false>(p, dev, ta, tb, td, stream);
+        return per_col ? launch_variant<256, 4, true>(p, dev, ta, tb, td, stream)
+                       : launch_variant<256, 4, false>(p, dev, ta, tb, td, stream);
     case 128:
-        return per_col ? launch_variant<128, 6, true, false>(p, dev, ta, tb, td, stream)
-                       : launch_variant<128, 6, false, false>(p, dev, ta, tb, td, stream);
+        return per_col ? launch_variant<128, 6, true>(p, dev, ta, tb, td, stream)
+                       : launch_variant<128, 6, false>(p, dev, ta, tb, td, stream);
     case 64:
-        return per_col ? launch_variant<64, 8, true, false>(p, dev, ta, tb, td, stream)
-                       : launch_variant<64, 8, false, false>(p, dev, ta, tb, td, stream);
+        return per_col ? launch_variant<64, 8, true>(p, dev, ta, tb, td, stream)
+                       : launch_variant<64, 8, false>(p, dev, ta, tb, td, stream);
     default:
-        return per_col ? launch_variant<32, 9, true, false>(p, dev, ta, tb, td, stream)
-                       : launch_variant<32, 9, false, false>(p, dev, ta, tb, td, stream);
+        return per_col ? launch_variant<32, 9, true>(p, dev, ta, tb, td, stream)
+                       : launch_variant<32, 9, false>(p, dev, ta, tb, td, stream);
     }
 }
 

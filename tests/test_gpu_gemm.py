@@ -125,10 +125,11 @@ def test_many_tiles_persistent_loop():
     run_wgrad(1024, 2048, 4096, 7, sample=2048)
 
 
-def test_pair_path_odd_tiles_and_ragged_rows():
-    """Problems large enough for the CTA-pair kernel, with an odd number of
-    128-column tiles (the second CTA of the last pair lies wholly outside the
-    output) and a ragged last row tile."""
+def test_odd_tile_counts_and_ragged_rows():
+    """Many tiles with an odd number of 128- and 256-column tiles per row of
+    tiles and a ragged last row tile (19207 = 150 x 128 + 7 rows): the
+    persistent loop's last wave is partial and its last tiles are clipped on
+    both axes."""
     run_fprop(19207, 384, 256, 41, sample=4096)
     run_dgrad(19207, 256, 384, 42, sample=4096)
     run_wgrad(256, 19200, 384, 43, sample=4096)

@@ -7,7 +7,9 @@ the runtime only when a call is made).
 """
 from __future__ import annotations
 
+import hashlib
 import os
+import platform
 import shutil
 import subprocess
 import sys
@@ -37,17 +39,36 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found")
 
 
-def _newest_input() -> float:
+STAMP_PATH = LIB_PATH + ".sha256"
+
+
+def _fingerprint(cc: str) -> str:
+    """SHA-256 of everything the library is built from: the sources and
+    headers, this script (flags), the compiler's version and the host
+    machine type (a library built on another architecture is never reused)."""
+    h = hashlib.sha256()
     files = [os.path.join(CSRC, f) for f in SOURCES + HEADERS] + [os.path.join(INCLUDE, "jetfp8.h"),
                                                                   os.path.abspath(__file__)]
-    return max(os.path.getmtime(f) for f in files)
+    for f in files:
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    ver = subprocess.run([cc, "--version"], capture_output=True, text=True).stdout
+    h.update(ver.encode())
+    h.update(platform.machine().encode())
+    return h.hexdigest()
 
 
 def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    if not force and os.path.exists(LIB_PATH) and os.path.getmtime(LIB_PATH) >= _newest_input():
-        return LIB_PATH
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    """Compile and link ``libjetfp8.so`` unless the library on disk was built
+    from exactly the current inputs (same fingerprint); returns its path."""
     cc = nvcc()
+    fp = _fingerprint(cc)
+    if not force and not ptxas_info and os.path.exists(LIB_PATH) and os.path.exists(STAMP_PATH):
+        with open(STAMP_PATH) as f:
+            if f.read().strip() == fp:
+                return LIB_PATH
+    os.makedirs(BUILD_DIR, exist_ok=True)
     extra = ["-Xptxas", "-v"] if ptxas_info else []
 
     def compile_one(src):
@@ -69,6 +90,8 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     if res.returncode != 0:
         raise RuntimeError(f"link failed:\n{res.stdout}\n{res.stderr}")
     os.replace(tmp, LIB_PATH)
+    with open(STAMP_PATH, "w") as f:
+        f.write(fp + "\n")
     return LIB_PATH
 
 

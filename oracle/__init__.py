@@ -53,14 +53,33 @@ _CFLAGS = ["-O2", "-std=c99", "-fPIC", "-shared", "-fno-fast-math",
 _lib = None
 
 
+def _fingerprint() -> str:
+    """SHA-256 of the C source, the flags, gcc's version and the machine type."""
+    import hashlib
+    import platform
+    h = hashlib.sha256()
+    with open(_SRC, "rb") as f:
+        h.update(f.read())
+    h.update(" ".join(_CFLAGS).encode())
+    h.update(subprocess.run(["gcc", "--version"], capture_output=True, text=True).stdout.encode())
+    h.update(platform.machine().encode())
+    return h.hexdigest()
+
+
 def build(force: bool = False) -> str:
-    """Compile the C oracle into ``oracle/libjetfp8_oracle.so`` (gcc)."""
-    if (not force and os.path.exists(_LIB_PATH)
-            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
-        return _LIB_PATH
+    """Compile the C oracle into ``oracle/libjetfp8_oracle.so`` (gcc) unless
+    the library on disk was built from exactly the current inputs."""
+    fp = _fingerprint()
+    stamp = _LIB_PATH + ".sha256"
+    if not force and os.path.exists(_LIB_PATH) and os.path.exists(stamp):
+        with open(stamp) as f:
+            if f.read().strip() == fp:
+                return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
     subprocess.check_call(["gcc", *_CFLAGS, "-o", tmp, _SRC, "-lm"])
     os.replace(tmp, _LIB_PATH)
+    with open(stamp, "w") as f:
+        f.write(fp + "\n")
     return _LIB_PATH
 
 

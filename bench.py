@@ -48,7 +48,7 @@ KERNELS = ("quant_w", "quant_x_dual", "quant_dy_dual", "fprop", "dgrad", "wgrad"
 # DRAM traffic of the dominant kernel (gemm_kernel<256,4,0,0>: the Fprop and Dgrad
 # launches), from one ncu capture of this step (dram__bytes_read.sum +
 # dram__bytes_write.sum per launch, averaged over the step's four Fprop and four Dgrad
-# launches, caches left warm as in the step; profiles/train8b_gemm_traffic.md).  It
+# launches, caches left warm as in the step).  It
 # describes the kernel built from the sources whose SHA-256 is recorded here (the
 # kernel and its inline-PTX helpers) and is reported as null once they differ.
 GEMM_TRAFFIC = {"bytes_per_launch": 956.1e6,
@@ -71,8 +71,8 @@ def gemm_traffic():
     the kernel's sources differ from those the bytes were captured on."""
     if gemm_sources_sha256() == GEMM_TRAFFIC["sha256"]:
         return (GEMM_TRAFFIC["bytes_per_launch"],
-                "DRAM bytes per launch (read + write, ncu, average of the 8 launches), "
-                "profiles/train8b_gemm_traffic.md")
+                "DRAM bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum, "
+                "average of the 8 launches)")
     return None, "null: the GEMM sources differ from those the traffic was captured on"
 
 

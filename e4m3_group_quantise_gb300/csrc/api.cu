@@ -170,7 +170,7 @@ JETFP8_API const char *jetfp8_status_string(jetfp8_status status)
 
 JETFP8_API jetfp8_status jetfp8_quantize_act(const void *x, int64_t M, int64_t K, uint8_t *q, float *s, void *stream)
 {
-    if (M < 0 || K <= 0 || K % 128 != 0 || !dims_ok(M, K) || K / 1024 > 65535)
+    if (M < 0 || K <= 0 || K % 128 != 0 || !dims_ok(M, K) || (K + 1023) / 1024 > 65535)   // grid y = ceil(K / 1024)
         return JETFP8_ERR_SHAPE;
     if (M == 0)
         return JETFP8_OK;

@@ -2,9 +2,9 @@
 //
 // Jet-RL (technical summaries on gist.science, "Schéma de Quantification"):
 // activations and gradients use 1x128 groups, weights 128x128 blocks, and the
-// WGrad operands 128x1 groups along the token axis ("1x128 et 128x1 pour
-// WGrad"), which the transposed quantiser writes out as 1x128 groups of the
-// transposed tensor.  Per group: amax = max |x|, s = amax / 448 (IEEE fp32
+// WGrad operands 1x128 / 128x1 groups, read here as groups of 128 tokens
+// along the token axis, which the transposed quantiser writes out as 1x128
+// groups of the transposed tensor.  Per group: amax = max |x|, s = amax / 448 (IEEE fp32
 // division), code = E4M3(RNE, saturating)(x / s) (IEEE fp32 division); a
 // zero group stores s = 0 and codes 0x00.
 //
@@ -357,8 +357,13 @@ quantize_act_dual_kernel(const __grid_constant__ CUtensorMap tmap_x, int64_t M, 
                          static_cast<int32_t>(m0));
     }
     const bool landed = ptx::mbar_wait(&sm.bar, 0, nullptr, err, ERRBIT_QUANT, 2000000000ull);
-    if (__syncthreads_or(!landed))
+    if (__syncthreads_or(!landed)) {
+        // the block gives up, but the copies it started must not land in
+        // shared memory after it has gone: one more bounded wait for them
+        if (threadIdx.x == 0)
+            ptx::mbar_wait(&sm.bar, 0, nullptr, err, ERRBIT_DRAIN, 2000000000ull);
         return;
+    }
 
     // ---- rows: 16 per warp, 8 per step; four lanes per row, 32 values each
     //      (16-byte chunks sub, sub+4, sub+8, sub+12 of the row's 256 bytes)

@@ -17,7 +17,7 @@
  *   - "Architecture Centrale" / "Arquitetura Central": rollout and training
  *     forward share one quantisation flow; master weights are BF16.
  * The pages say only "FP8".  Where they are silent this file takes the
- * readings below (also listed in the design notes):
+ * readings below:
  *   - format: OCP FP8 E4M3 "FN" (bias 7, no infinities, S.1111.111 = NaN,
  *     largest finite 448);
  *   - scale: one fp32 per group, s = amax / 448 as one IEEE fp32 division;
@@ -141,7 +141,8 @@ void jo_quantize_act(const uint16_t *x, int64_t M, int64_t K, uint8_t *q, float 
 /*
  * The WGrad operand: groups of 128 consecutive rows (tokens) of one column
  * ("128x1" in the [M][C] layout), written transposed so that each group is
- * 1x128 in the output ("1x128 et 128x1 pour WGrad").
+ * 1x128 in the output (the summaries give WGrad 1x128 and 128x1 groups,
+ * "Schéma de Quantification").
  *   x : bf16 bits [M][C]         qt : codes [C][M]
  *   st: fp32 [M/128][C]  (st[g*C + c] belongs to column c, row group g)
  */

@@ -70,6 +70,9 @@ def test_quantize_act_validation(lib):
     assert f(A16, 4, 128, A16 + 64, C16, None) == J.ERR_INVALID_VALUE  # q overlaps x
     assert f(A16, 4, 128, B16, B16 + 256, None) == J.ERR_INVALID_VALUE  # s overlaps q
     assert f(A16, 1 << 31, 128, B16, C16, None) == J.ERR_SHAPE     # row count limit
+    # the launch grid has ceil(K / 1024) blocks along y (at most 65535): the
+    # first K past that limit is a shape error, not a failed launch
+    assert f(A16, 1, 65535 * 1024 + 128, B16, C16, None) == J.ERR_SHAPE
 
 
 def test_quantize_transposed_validation(lib):

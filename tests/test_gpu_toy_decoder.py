@@ -70,7 +70,7 @@ def test_bf16_vs_fp8_mismatch_by_length(model, T):
     the FP8 forward, on the same weights, at growing sequence length.  The
     FP8 rollout and the FP8 training forward stay bit-identical at every
     length (mismatch exactly 0); BF16 against FP8 differs.  The figures are
-    printed (pytest -s) and recorded with the design notes."""
+    printed (pytest -s) for the record."""
     g = torch.Generator().manual_seed(100 + T)
     t = torch.randint(0, 4096, (1, T), generator=g).cuda()
     with torch.no_grad():

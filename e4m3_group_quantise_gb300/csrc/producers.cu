@@ -3,12 +3,17 @@
 // "Implémentation": fused activation / RMSNorm kernels feeding the FP8
 // GEMMs), so the bf16 intermediate need not make a round trip through HBM.
 //
-// The pages give no arithmetic for these operators; this library defines it
-// step by step: every operation below is one IEEE fp32 operation in a fixed
-// order (written with the _rn intrinsics and fmaf, so the compiler never
-// contracts a multiply and an add), the result is rounded to bf16 (nearest
-// even), and that bf16 value is quantised exactly as jetfp8_quantize_act
-// quantises it.  The optional bf16 output is the same rounded value.
+// The pages give no arithmetic for these operators, so their textbook
+// definitions are the contract: RMSNorm y = x / sqrt(mean(x^2) + eps) * gamma
+// and SwiGLU y = silu(g) * u, each bf16 result within one bf16 ulp of the
+// exact value (for gates below -87, where the fp32 sigmoid underflows, within
+// 2^-119 |u|; rows whose sum of squares overflows fp32 are outside the
+// domain).  The kernels evaluate them in fp32 in a fixed order (every
+// operation one IEEE fp32 operation, written with the _rn intrinsics and
+// fmaf so that nothing is contracted), so a row's result never depends on
+// the launch or on the other rows; the bf16 value (nearest even) is then
+// quantised exactly as jetfp8_quantize_act quantises it, and the optional
+// bf16 output is that same value.
 //
 // Layout of the work: a warp takes a 256-column chunk of one row, lane l the
 // eight values 8l .. 8l+7, loaded and stored as 16-byte vectors.  A 1x128

@@ -85,3 +85,11 @@ def grad_output(M: int, N: int, seed: int, index: int = 0, device="cpu", sigma: 
 def bf16_bits(t: torch.Tensor):
     """CPU uint16 numpy view of a bf16 tensor's bit patterns (for the oracle)."""
     return t.detach().contiguous().cpu().view(torch.int16).numpy().view("uint16")
+
+
+def np_f32_to_bf16_bits(v):
+    """bf16 bit patterns (uint16 numpy) of fp32 values, rounded to nearest even
+    by PyTorch's own conversion."""
+    import numpy as np
+    t = torch.from_numpy(np.ascontiguousarray(v, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view("uint16")

@@ -118,12 +118,12 @@ JETFP8_API jetfp8_status jetfp8_quantize_act_dual(const void *x, int64_t M, int6
  * Fused RMSNorm producer: the 1x128 FP8 input of the next linear layer
  * straight from the residual stream (Jet-RL, "Implémentation": fused
  * activation / RMSNorm kernels in front of the FP8 GEMMs).  Per row:
- *   ms = (sum of x_i^2) / H, rstd = 1 / sqrt(ms + eps),
- *   y_i = bf16((x_i * rstd) * gamma_i)   (round to nearest even),
- * each step one IEEE fp32 operation; the sum of squares runs in a fixed
- * order (32 partial sums, partial l over the 8-element chunks 32 j + l in
- * increasing j, combined pairwise at distances 16, 8, 4, 2, 1).  The codes
- * and scales are exactly those jetfp8_quantize_act gives for y.
+ *   y_i = x_i / sqrt( (1/H) sum_j x_j^2 + eps ) * gamma_i,
+ * returned as bf16 within one bf16 ulp of the exact value (computed in
+ * fp32 in a fixed order, so a row's bits never depend on the launch or the
+ * other rows).  Rows whose sum of squares overflows fp32 are outside the
+ * domain.  The codes and scales are exactly those jetfp8_quantize_act
+ * gives for the returned bf16 y.
  *   x     : bf16 [M][H]                    (input)
  *   gamma : bf16 [H]                       (input)
  *   eps   : finite, >= 0
@@ -139,11 +139,11 @@ JETFP8_API jetfp8_status jetfp8_rmsnorm_quantize_act(const void *x, const void *
  * Fused SwiGLU producer: the 1x128 FP8 input of the down projection from
  * the gate_up output (Jet-RL, "Implémentation": fused activation kernels).
  * gu holds gate in columns 0..I-1 and up in columns I..2I-1 of each row;
- *   y = bf16( (g * (1 / (1 + e^-g))) * u )
- * with one IEEE fp32 operation per step and e^x this library's own fp32
- * exponential: Cody-Waite reduction by ln 2 and a degree-7 Taylor
- * polynomial (within 2 ulp of e^x; +inf for x >= 89, +0 for x < -87).
- * The codes and scales are exactly those jetfp8_quantize_act gives for y.
+ *   y = silu(g) * u = g / (1 + e^-g) * u,
+ * returned as bf16 within one bf16 ulp of the exact value (fp32 in a fixed
+ * order, with this library's own fp32 e^x); for g < -87, where the fp32
+ * sigmoid underflows, within 2^-119 |u| of it.  The codes and scales are
+ * exactly those jetfp8_quantize_act gives for the returned bf16 y.
  *   gu   : bf16 [M][2I]                    (input)
  *   q, s : uint8 [M][I], fp32 [I/128][M], or both NULL
  *   y    : bf16 [M][I] or NULL
@@ -219,8 +219,8 @@ JETFP8_API jetfp8_status jetfp8_gemm_wgrad(const uint8_t *qdyt, const float *sdy
 
 /*
  * Test hook for the conversion every quantiser ends in: codes[i] = the
- * OCP E4M3 code (round to nearest even, saturating to +-448, NaN -> 0x7F or
- * 0xFF by sign) that the GPU's E4M3 conversion gives for the fp32 value whose
+ * OCP E4M3 code (round to nearest even, saturating to +-448, every NaN ->
+ * 0x7F, whatever its sign) that the GPU's E4M3 conversion gives for the fp32 value whose
  * bit pattern is first + i, i = 0 .. count-1.  Lets a test compare the
  * hardware conversion with a reference over all 2^32 fp32 patterns, in
  * chunks.

@@ -21,11 +21,13 @@ What it computes (Jet-RL technical summaries, gist.science fr/pt,
                                  optional transposed codes.
   * ``gemm_fprop/dgrad/wgrad``  exact fp64 sums of dequantised products,
                                  plus the sum of |products| for tolerances.
-  * ``rmsnorm``, ``swiglu``     the bf16 producers fused in front of the
-                                 linear layers ("Implémentation": fused
-                                 activation / RMSNorm kernels), defined step
-                                 by step in fp32 in the C file; their FP8
-                                 form is ``quantize_act`` of the result.
+  * ``rmsnorm``, ``swiglu``     the operators fused in front of the linear
+                                 layers ("Implémentation": fused activation /
+                                 RMSNorm kernels), their textbook definitions
+                                 evaluated in fp64; a kernel's bf16 output is
+                                 checked against them to within one bf16
+                                 ulp and its FP8 form against
+                                 ``quantize_act`` of that bf16 output.
 Readings the pages leave open (format E4M3-FN, s = amax/448 in fp32, RNE,
 saturating, zero group -> s = 0 and codes 0) are stated in the C file.
 
@@ -105,12 +107,8 @@ def _load():
     lib.jo_quantize_weight.argtypes = [P, I, I, P, P, P]
     for name in ("jo_gemm_fprop", "jo_gemm_dgrad", "jo_gemm_wgrad"):
         getattr(lib, name).argtypes = [P, P, P, P, I, I, I, P, P, I, P, P]
-    lib.jo_exp.restype = ctypes.c_float
-    lib.jo_exp.argtypes = [ctypes.c_float]
-    lib.jo_exp_array.argtypes = [P, I, P]
-    lib.jo_float_to_bf16_array.argtypes = [P, I, P]
-    lib.jo_swiglu.argtypes = [P, I, I, P]
-    lib.jo_rmsnorm.argtypes = [P, P, ctypes.c_float, I, I, P]
+    lib.jo_swiglu_f64.argtypes = [P, I, I, P]
+    lib.jo_rmsnorm_f64.argtypes = [P, P, ctypes.c_double, I, I, P]
     _lib = lib
     return lib
 
@@ -344,40 +342,38 @@ def gemm_within_tolerance(got, ref, abssum, rel: float = 1e-3):
     return ok, float(ratio.ravel()[worst]), worst
 
 
+def bf16_within_ulp(got_bits, ref, ulps: float = 1.0):
+    """The producers' bar: a bf16 result (bit patterns) within ``ulps`` bf16
+    ulps of the fp64 value, per element.  Returns (all_ok, worst error in
+    ulps, flat index of the worst)."""
+    got = bf16_bits_to_f32(got_bits).astype(np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    err = np.abs(got - ref) / bf16_ulp(ref)
+    if err.size == 0:
+        return True, 0.0, -1
+    worst = int(np.nanargmax(np.where(np.isnan(err), np.inf, err)))
+    ok = bool(np.all(err <= ulps))
+    return ok, float(err.ravel()[worst]), worst
+
+
 # ------------------------------------------------------------ producers
-def exp_f32(x) -> np.ndarray:
-    """The oracle's fp32 e^x (Cody-Waite reduction + degree-7 Taylor)."""
-    lib = _load()
-    v = np.ascontiguousarray(x, dtype=np.float32)
-    out = np.empty(v.shape, dtype=np.float32)
-    lib.jo_exp_array(_ptr(v), v.size, _ptr(out))
-    return out
-
-
-def float_to_bf16_bits(x) -> np.ndarray:
-    """fp32 -> bf16 bit patterns, round to nearest even."""
-    lib = _load()
-    v = np.ascontiguousarray(x, dtype=np.float32)
-    out = np.empty(v.shape, dtype=np.uint16)
-    lib.jo_float_to_bf16_array(_ptr(v), v.size, _ptr(out))
-    return out
-
-
 def swiglu(gu, threads: int = 1) -> np.ndarray:
-    """gate_up output bf16 [M, 2I] -> y bf16 bits [M, I] = silu(gate) * up."""
+    """gate_up output bf16 [M, 2I] -> y float64 [M, I] = silu(gate) * up,
+    evaluated in fp64 (the kernel's bf16 y is checked against it to within
+    one bf16 ulp)."""
     lib = _load()
     g = _as_bf16_bits(gu)
     M, I2 = g.shape
     if I2 % 2:
         raise ValueError("gate_up width must be even")
     I = I2 // 2
-    y = np.empty((M, I), dtype=np.uint16)
+    y = np.empty((M, I), dtype=np.float64)
 
     def work(r):
         a, b = r
         sub = np.ascontiguousarray(g[a:b])
-        out = np.empty((b - a, I), dtype=np.uint16)
-        lib.jo_swiglu(_ptr(sub), b - a, I, _ptr(out))
+        out = np.empty((b - a, I), dtype=np.float64)
+        lib.jo_swiglu_f64(_ptr(sub), b - a, I, _ptr(out))
         y[a:b] = out
 
     chunks = _row_chunks(M, max(1, threads)) if M else []
@@ -391,20 +387,22 @@ def swiglu(gu, threads: int = 1) -> np.ndarray:
 
 
 def rmsnorm(x, gamma, eps: float, threads: int = 1) -> np.ndarray:
-    """x bf16 [M, H], gamma bf16 [H] -> y bf16 bits [M, H] (H % 256 == 0)."""
+    """x bf16 [M, H], gamma bf16 [H] -> y float64 [M, H], RMSNorm in fp64.
+    ``eps`` is taken at fp32 precision (the C-ABI passes it as a float)."""
     lib = _load()
     xb = _as_bf16_bits(x)
     gb = np.ascontiguousarray(_as_bf16_bits(gamma).reshape(-1))
     M, H = xb.shape
-    if H % 256 or gb.size != H:
-        raise ValueError("H must be a multiple of 256 and gamma must have H entries")
-    y = np.empty((M, H), dtype=np.uint16)
+    if gb.size != H:
+        raise ValueError("gamma must have H entries")
+    eps64 = float(np.float32(eps))
+    y = np.empty((M, H), dtype=np.float64)
 
     def work(r):
         a, b = r
         sub = np.ascontiguousarray(xb[a:b])
-        out = np.empty((b - a, H), dtype=np.uint16)
-        lib.jo_rmsnorm(_ptr(sub), _ptr(gb), ctypes.c_float(eps), b - a, H, _ptr(out))
+        out = np.empty((b - a, H), dtype=np.float64)
+        lib.jo_rmsnorm_f64(_ptr(sub), _ptr(gb), ctypes.c_double(eps64), b - a, H, _ptr(out))
         y[a:b] = out
 
     chunks = _row_chunks(M, max(1, threads)) if M else []

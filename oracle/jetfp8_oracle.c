@@ -326,144 +326,50 @@ int64_t jo_e4m3_encode_check_range(uint32_t lo, uint64_t count, const uint8_t *c
 /*                                                                    */
 /* The pages (technical summaries, "Implémentation") name fused      */
 /* activation / RMSNorm kernels that emit the FP8 input of the next  */
-/* GEMM, without their arithmetic.  The definitions below are this   */
-/* library's: every step is one IEEE fp32 operation (+, *, /, sqrt,   */
-/* fmaf, rint) in the stated order, so that the CUDA kernels can      */
-/* reproduce them bit for bit; the bf16 result is then quantised      */
-/* exactly like jo_quantize_act.                                      */
+/* GEMM, without their arithmetic.  The oracle takes the operators'  */
+/* textbook definitions and evaluates them in fp64 (double), in the  */
+/* plainest order; the bf16 value a kernel produces is checked        */
+/* against this to within one bf16 ulp, and the kernel's FP8 codes    */
+/* against jo_quantize_act of that bf16 value.                        */
 /* ------------------------------------------------------------------ */
 
-/* fp32 -> bf16, round to nearest, ties to even (NaN kept quiet). */
-uint16_t jo_float_to_bf16(float f)
-{
-    uint32_t b;
-    memcpy(&b, &f, sizeof b);
-    if ((b & 0x7F800000u) == 0x7F800000u && (b & 0x007FFFFFu) != 0u)
-        return (uint16_t)((b >> 16) | 0x0040u);
-    b += 0x7FFFu + ((b >> 16) & 1u);      /* carries into bit 16 exactly when rounding up */
-    return (uint16_t)(b >> 16);
-}
-
-static float pow2f_normal(int k)           /* 2^k for -126 <= k <= 127, exact */
-{
-    uint32_t bits = (uint32_t)(k + 127) << 23;
-    float f;
-    memcpy(&f, &bits, sizeof f);
-    return f;
-}
-
 /*
- * e^x in fp32: Cody-Waite range reduction x = n ln2 + r (|r| <= ln2 / 2,
- * n = rint(x / ln2)) and e^r by its degree-7 Taylor polynomial in Horner
- * form with fused multiply-adds; e^x = e^r 2^n.  ln2 is split into a head
- * with 16 significant bits (45426 / 2^16, so n * head is exact for |n| <
- * 256) and the fp32-rounded remainder.  x >= 89 gives +inf, x < -87 gives
- * +0 (results below the smallest normal are not produced); between those
- * bounds the final scaling by 2^n may still overflow to +inf.
+ * RMSNorm (root-mean-square layer normalisation, Zhang and Sennrich 2019)
+ * of x bf16 [M][H] with gain gamma bf16 [H]:
+ *   y_i = x_i / sqrt( (1/H) sum_j x_j^2 + eps ) * gamma_i,
+ * every operation in double, the sum over the row in natural order.
+ *   y : fp64 [M][H]
  */
-float jo_exp(float x)
+void jo_rmsnorm_f64(const uint16_t *x, const uint16_t *gamma, double eps, int64_t M, int64_t H, double *y)
 {
-    const float log2e = 1.44269502f;               /* fp32(1 / ln 2) */
-    const float ln2_hi = 0.693145751953125f;       /* 45426 / 65536 */
-    const float ln2_lo = 1.42860677e-06f;          /* fp32(ln 2 - ln2_hi) */
-    const float c7 = 0.000198412701f, c6 = 0.00138888892f, c5 = 0.00833333377f,
-                c4 = 0.0416666679f, c3 = 0.166666672f, c2 = 0.5f;   /* fp32(1/k!) */
-    float n, r, p;
-    int ni, n1;
-
-    if (x != x)
-        return x;
-    if (x >= 89.0f)
-        return INFINITY;
-    if (x < -87.0f)
-        return 0.0f;
-    n = rintf(x * log2e);
-    r = fmaf(-n, ln2_hi, x);
-    r = fmaf(-n, ln2_lo, r);
-    p = c7;
-    p = fmaf(p, r, c6);
-    p = fmaf(p, r, c5);
-    p = fmaf(p, r, c4);
-    p = fmaf(p, r, c3);
-    p = fmaf(p, r, c2);
-    p = fmaf(p, r, 1.0f);
-    p = fmaf(p, r, 1.0f);
-    ni = (int)n;                                   /* -126 .. 128 */
-    n1 = ni / 2;
-    return (p * pow2f_normal(n1)) * pow2f_normal(ni - n1);
+    for (int64_t m = 0; m < M; ++m) {
+        const uint16_t *row = x + m * H;
+        double sum = 0.0, rms;
+        for (int64_t j = 0; j < H; ++j) {
+            double v = (double)jo_bf16_to_float(row[j]);
+            sum += v * v;
+        }
+        rms = sqrt(sum / (double)H + eps);
+        for (int64_t i = 0; i < H; ++i)
+            y[m * H + i] = (double)jo_bf16_to_float(row[i]) / rms * (double)jo_bf16_to_float(gamma[i]);
+    }
 }
 
 /*
  * SwiGLU of a gate_up projection output, gu bf16 [M][2I] (gate = columns
  * 0..I-1, up = columns I..2I-1):
- *   y = bf16( silu(g) * u ),  silu(g) = g * (1 / (1 + e^-g))
- * with g, u the fp32 values of the bf16 inputs, e^-g = jo_exp(-g), and the
- * operations in exactly this order (add, divide, multiply, multiply).
+ *   y = silu(g) * u,   silu(g) = g * sigmoid(g) = g / (1 + e^-g),
+ * in double with the C library's exp.
+ *   y : fp64 [M][I]
  */
-void jo_swiglu(const uint16_t *gu, int64_t M, int64_t I, uint16_t *y)
+void jo_swiglu_f64(const uint16_t *gu, int64_t M, int64_t I, double *y)
 {
     for (int64_t m = 0; m < M; ++m) {
         const uint16_t *row = gu + m * 2 * I;
         for (int64_t i = 0; i < I; ++i) {
-            float g = jo_bf16_to_float(row[i]);
-            float u = jo_bf16_to_float(row[I + i]);
-            float sig = 1.0f / (1.0f + jo_exp(-g));
-            float silu = g * sig;
-            y[m * I + i] = jo_float_to_bf16(silu * u);
+            double g = (double)jo_bf16_to_float(row[i]);
+            double u = (double)jo_bf16_to_float(row[I + i]);
+            y[m * I + i] = g / (1.0 + exp(-g)) * u;
         }
     }
-}
-
-/*
- * RMSNorm of x bf16 [M][H] with gain gamma bf16 [H] (H a multiple of 256):
- *   ms   = (sum of x_i^2) / H,   rstd = 1 / sqrt(ms + eps),
- *   y_i  = bf16( (x_i * rstd) * gamma_i ).
- * The sum of squares has a fixed order (the one a 32-lane warp reading
- * 8-element chunks produces): lane l (0..31) sums, in order, the squares of
- * elements 8 (32 j + l) .. 8 (32 j + l) + 7 for j = 0, 1, ..., H/256 - 1;
- * the 32 partial sums are then combined pairwise, partner distance 16, 8,
- * 4, 2, 1 (partial[l] = partial[l] + partial[l ^ d]; every lane ends with
- * the same total).  Each x_i^2 is exact in fp32 (bf16 has 8 significant
- * bits); every addition rounds.  Division, square root and the two
- * multiplications are single IEEE fp32 operations.
- */
-void jo_rmsnorm(const uint16_t *x, const uint16_t *gamma, float eps, int64_t M, int64_t H, uint16_t *y)
-{
-    for (int64_t m = 0; m < M; ++m) {
-        const uint16_t *row = x + m * H;
-        float part[32], tmp[32];
-        for (int l = 0; l < 32; ++l) {
-            float acc = 0.0f;
-            for (int64_t j = 0; j < H / 256; ++j)
-                for (int e = 0; e < 8; ++e) {
-                    float v = jo_bf16_to_float(row[8 * (32 * j + l) + e]);
-                    acc = acc + v * v;
-                }
-            part[l] = acc;
-        }
-        for (int d = 16; d >= 1; d /= 2) {
-            for (int l = 0; l < 32; ++l)
-                tmp[l] = part[l] + part[l ^ d];
-            memcpy(part, tmp, sizeof part);
-        }
-        float ms = part[0] / (float)H;
-        float rstd = 1.0f / sqrtf(ms + eps);
-        for (int64_t i = 0; i < H; ++i) {
-            float v = jo_bf16_to_float(row[i]);
-            float g = jo_bf16_to_float(gamma[i]);
-            y[m * H + i] = jo_float_to_bf16((v * rstd) * g);
-        }
-    }
-}
-
-void jo_exp_array(const float *x, int64_t n, float *out)
-{
-    for (int64_t i = 0; i < n; ++i)
-        out[i] = jo_exp(x[i]);
-}
-
-void jo_float_to_bf16_array(const float *x, int64_t n, uint16_t *out)
-{
-    for (int64_t i = 0; i < n; ++i)
-        out[i] = jo_float_to_bf16(x[i]);
 }

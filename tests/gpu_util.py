@@ -30,11 +30,18 @@ def assert_bitexact(got: torch.Tensor, want: np.ndarray, what: str):
                           f"{[(int(g[tuple(i)]), int(want[tuple(i)])) for i in bad[:5]]}"
 
 
+# (case, worst error/bound, elements compared) of every GEMM parity check in
+# this session; printed at the end of the run (see conftest.py) so that a
+# shrinking margin shows up before it turns into a failure
+GEMM_MARGINS = []
+
+
 def assert_gemm_close(got: torch.Tensor, ref: np.ndarray, asum: np.ndarray, what: str, rows=None, cols=None):
     g = got.float().cpu().numpy()
     if rows is not None:
         g = g[rows, cols]
     ok, worst, idx = oracle.gemm_within_tolerance(g, ref, asum)
+    GEMM_MARGINS.append((what, worst, int(np.asarray(ref).size)))
     assert ok, f"{what}: outside tolerance, worst error/bound {worst:.4g} at flat index {idx} " \
                f"(got {g.ravel()[idx]!r}, ref {np.asarray(ref).ravel()[idx]!r})"
     return worst

@@ -15,6 +15,14 @@ Jet-RL (technical summaries on gist.science, "Architecture Centrale" and
     boundary (1x128 for DGrad, 128x1 for WGrad), and DGrad / WGrad run in FP8.
 Only tensor allocation and autograd wiring live here; every arithmetic step
 is a call into the CUDA library.
+
+Errors: the calls raise on any argument or launch error.  A kernel whose
+bounded wait on an asynchronous copy or a tensor-core barrier gives up does
+not hang: it records the failure in the device's error word and leaves its
+output incomplete.  Reading that word needs a synchronisation, so these layers
+never read it themselves; a training or rollout loop that must not continue
+on incomplete results calls ``jetfp8_poll_device_error()`` once per step
+(after the backward, or after a rollout batch) and stops on a non-zero status.
 """
 from __future__ import annotations
 

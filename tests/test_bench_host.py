@@ -38,9 +38,35 @@ def test_quantiser_bytes_per_element():
 
 def test_traffic_reported_only_for_captured_sources(monkeypatch):
     current = bench.gemm_sources_sha256()
+    table = {f"{k}:{p}": 1000.0 * (i + 1) for i, (k, p) in enumerate(
+        (k, p) for k in ("fprop", "dgrad") for p in bench.PROJ)}
+    monkeypatch.setitem(bench.GEMM_TRAFFIC, "per_launch_bytes", table)
     monkeypatch.setitem(bench.GEMM_TRAFFIC, "sha256", current)
     traffic, _ = bench.gemm_traffic()
-    assert traffic == bench.GEMM_TRAFFIC["bytes_per_launch"]
+    assert traffic == sum(table.values()) / len(table)
+    # a launch of the step without a capture: no figure
+    monkeypatch.setitem(bench.GEMM_TRAFFIC, "per_launch_bytes", dict(list(table.items())[1:]))
+    traffic, note = bench.gemm_traffic()
+    assert traffic is None and note.startswith("null")
+    # other sources than those captured: no figure
+    monkeypatch.setitem(bench.GEMM_TRAFFIC, "per_launch_bytes", table)
     monkeypatch.setitem(bench.GEMM_TRAFFIC, "sha256", "0" * 64)
     traffic, note = bench.gemm_traffic()
     assert traffic is None and note.startswith("null")
+
+
+def test_workloads_match_the_configured_shapes():
+    """train-8b: the four 8B projections at 16384 tokens; train-32b: the four
+    32B projections at 32768 tokens (2 x 16384)."""
+    w8, w32 = bench.WORKLOADS["train-8b"], bench.WORKLOADS["train-32b"]
+    assert w8["tokens"] == 16384 and w8["proj"] == {"qkv": (6144, 4096), "o": (4096, 4096),
+                                                     "gate_up": (28672, 4096), "down": (4096, 14336)}
+    assert w32["tokens"] == 32768 and w32["proj"] == {"qkv": (7168, 5120), "o": (5120, 5120),
+                                                       "gate_up": (55296, 5120), "down": (5120, 27648)}
+    assert w32["student_t"] and w32["outlier_scale"] == 100.0 and w32["dy_sigma"] == 1e-3
+    # 32B step: 3 GEMMs x 2MNK over the four projections, about 95.9 TFLOP
+    assert abs(bench.gemm_flops(w32["proj"], w32["tokens"]) / 1e12 - 95.9) < 0.1
+
+
+def test_burst_peak_is_twice_the_bf16_burst():
+    assert bench.fp8_burst_peak({"bf16_tflops": 1880.6}) == 2 * 1880.6

@@ -74,7 +74,14 @@ template <> struct RegSplit<64> { static constexpr uint32_t CTRL = 88, PROMO = 2
 template <> struct RegSplit<32> { static constexpr uint32_t CTRL = 88, PROMO = 200; };
 static_assert(128 * RegSplit<256>::CTRL + 256 * RegSplit<256>::PROMO <= NUM_THREADS * 168, "register split");
 static_assert(128 * RegSplit<128>::CTRL + 256 * RegSplit<128>::PROMO <= NUM_THREADS * 168, "register split");
-constexpr int GROUP_M = 16;              // tile rasterisation: m-tiles per band
+// Tile rasterisation: the part of an operand that a band of tiles reuses
+// across waves is kept to this many bytes.  Measured on GB300 (one launch per
+// ncu capture): a 25 MB operand reused by every wave is read from DRAM once,
+// a 59-67 MB one 10 to 30 times -- lines that every SM reads are held in both
+// halves of the L2, so reuse across waves holds only for about a quarter of
+// the L2's nominal size.
+constexpr int64_t L2_BAND_BYTES = int64_t{30} << 20;
+constexpr int BALANCED_BAND_M = 16;      // bands of 16 m-tiles when no operand slice can stay in L2
 constexpr uint64_t WAIT_TIMEOUT_NS = 2000000000ull;   // 2 s
 
 struct KernelArgs {
@@ -86,6 +93,11 @@ struct KernelArgs {
     uint32_t *err;
     int32_t rows, cols, groups;
     int32_t tiles_m, tiles_n;
+    int32_t band;         // tile rasterisation: tiles per band along the banded axis (see launch_gemm)
+    int32_t band_n;       // 0: bands of m-tiles, 1: bands of n-tiles
+    int32_t stream_a;     // 1: A's tiles are read once, load them with the evict-first L2 priority
+    int32_t stream_b;     // 1: the same for B
+    int32_t stream_d;     // 1: the output is larger than L2 can keep: store it with evict-first
 };
 
 template <int BN, int STAGES>
@@ -110,15 +122,24 @@ struct Smem {
     static constexpr uint32_t TOTAL = 1024 /* alignment slack */ + BAR_OFF + CTRL_BYTES;
 };
 
-__device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int &tm, int &tn)
+// Tile order: bands of `band` tiles along one axis, the banded axis varying
+// fastest inside a band, which then sweeps the whole other axis.  The
+// band's slice of its operand (band x 128 rows of A, or band x BN rows of B,
+// each over the whole contraction) is what consecutive waves reuse; the
+// other operand is read once per band.
+__device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int band, int band_n, int &tm,
+                                            int &tn)
 {
-    const int per_band = GROUP_M * tiles_n;
-    const int band = tile / per_band;
-    const int first_m = band * GROUP_M;
-    const int band_m = min(tiles_m - first_m, GROUP_M);
-    const int in_band = tile - band * per_band;
-    tm = first_m + in_band % band_m;
-    tn = in_band / band_m;
+    const int banded = band_n ? tiles_n : tiles_m;
+    const int other = band_n ? tiles_m : tiles_n;
+    const int per_band = band * other;
+    const int b = tile / per_band;
+    const int first = b * band;
+    const int width = min(banded - first, band);
+    const int in_band = tile - b * per_band;
+    const int u = first + in_band % width, v = in_band / width;
+    tm = band_n ? v : u;
+    tn = band_n ? u : v;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
@@ -198,7 +219,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     const int num_work = args.tiles_m * args.tiles_n;
     const int work_first = static_cast<int>(blockIdx.x);
     const int work_stride = static_cast<int>(gridDim.x);
-    auto coords = [&](int w, int &tm, int &tn) { tile_coords(w, args.tiles_m, args.tiles_n, tm, tn); };
+    auto coords = [&](int w, int &tm, int &tn) {
+        tile_coords(w, args.tiles_m, args.tiles_n, args.band, args.band_n, tm, tn);
+    };
 
     if (warp == PRODUCER_WARP) {
         if (lane == 0) {
@@ -239,6 +262,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                 int stage = 0;
                 uint32_t phase = 0;
                 uint32_t issued_mask = 0, issued_parity = 0;
+                const uint64_t pol_a = args.stream_a ? ptx::l2_policy_evict_first() : ptx::l2_policy_evict_normal();
+                const uint64_t pol_b = args.stream_b ? ptx::l2_policy_evict_first() : ptx::l2_policy_evict_normal();
                 int ss = 0;
                 uint32_t sphase = 0;
                 bool scale_pending = false;      // a scale copy this thread started may be in flight
@@ -274,8 +299,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                             break;
                         }
                         ptx::mbar_arrive_expect_tx(&full[stage], L::STAGE_BYTES);
-                        ptx::tma_load_2d(sA + stage * L::A_BYTES, &tmap_a, &full[stage], g * BK, tm * BM);
-                        ptx::tma_load_2d(sB + stage * L::B_BYTES, &tmap_b, &full[stage], g * BK, tn * BN);
+                        ptx::tma_load_2d_hint(sA + stage * L::A_BYTES, &tmap_a, &full[stage], g * BK, tm * BM, pol_a);
+                        ptx::tma_load_2d_hint(sB + stage * L::B_BYTES, &tmap_b, &full[stage], g * BK, tn * BN, pol_b);
                         issued_mask |= 1u << stage;
                         issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
                         if (++stage == STAGES) {
@@ -389,6 +414,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         const int quarter = warp & 3;                    // TMEM lanes 32*quarter .. +31
         const int row_in_tile = quarter * 32 + lane;
         uint8_t *out_stage = smem + L::OUT_OFF + (warp - FIRST_PROMO_WARP) * 2 * L::OUT_CHUNK_BYTES;
+        const uint64_t pol_d = args.stream_d ? ptx::l2_policy_evict_first() : ptx::l2_policy_evict_normal();
         uint32_t it = 0;
         int ss = 0;
         uint32_t sphase = 0;
@@ -572,7 +598,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                     ptx::fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        ptx::tma_store_2d(&tmap_d, chunk, col0 + 16 * c, tm * BM + quarter * 32);
+                        ptx::tma_store_2d_hint(&tmap_d, chunk, col0 + 16 * c, tm * BM + quarter * 32, pol_d);
                         ptx::bulk_commit();
                     }
                 }
@@ -613,6 +639,44 @@ cudaError_t launch_variant(const GemmProblem &p, const DeviceInfo &dev, const CU
     a.groups = static_cast<int32_t>(p.kdim / BK);
     a.tiles_m = static_cast<int32_t>((p.rows + BM - 1) / BM);
     a.tiles_n = static_cast<int32_t>((p.cols + BN - 1) / BN);
+    // Tile order and L2 priorities.  Every CTA of a wave walks the whole
+    // contraction, so an operand is fetched from DRAM once per wave that
+    // uses it unless it stays in L2 between waves.  Bands along m keep a
+    // band of A in L2 and read B once per band; bands along n the reverse.
+    // Each band's reused slice is at most L2_BAND_BYTES; the cheaper axis
+    // (reused operand once + the other once per band) is compared with the
+    // balanced order (bands of 16 m-tiles, every wave reading its own
+    // operand slices), and a band is used only when it promises under 0.8
+    // of the balanced order's bytes: with long contractions the slices that
+    // one wave streams are as large as the L2 and the reuse does not
+    // materialise (measured).  With a band, the operand read once per band
+    // is loaded with the evict-first priority so that it does not push the
+    // reused slice out.  The order never changes how an output element is
+    // reduced.
+    const int64_t a_bytes = p.rows * p.kdim, b_bytes = p.cols * p.kdim;
+    const int64_t a_tile = int64_t{BM} * p.kdim, b_tile = int64_t{BN} * p.kdim;
+    auto clamp_band = [](int64_t v, int64_t hi) { return v < 1 ? int64_t{1} : (v > hi ? hi : v); };
+    const int64_t band_m = clamp_band(L2_BAND_BYTES / a_tile, a.tiles_m);
+    const int64_t band_n = clamp_band(L2_BAND_BYTES / b_tile, a.tiles_n);
+    const int64_t cost_m = a_bytes + b_bytes * ((a.tiles_m + band_m - 1) / band_m);
+    const int64_t cost_n = b_bytes + a_bytes * ((a.tiles_n + band_n - 1) / band_n);
+    const int64_t bal_m = a.tiles_m < BALANCED_BAND_M ? a.tiles_m : BALANCED_BAND_M;
+    const int64_t bal_n_per_wave = (dev.sm_count + bal_m - 1) / bal_m;
+    const int64_t bal_n = bal_n_per_wave < a.tiles_n ? bal_n_per_wave : a.tiles_n;
+    const int64_t waves = (int64_t{a.tiles_m} * a.tiles_n + dev.sm_count - 1) / dev.sm_count;
+    const int64_t cost_bal = waves * (bal_m * a_tile + bal_n * b_tile);
+    const int64_t cost_band = cost_n < cost_m ? cost_n : cost_m;
+    a.stream_a = a.stream_b = 0;
+    if (5 * cost_band < 4 * cost_bal) {
+        a.band_n = cost_n < cost_m ? 1 : 0;
+        a.band = static_cast<int32_t>(a.band_n ? band_n : band_m);
+        a.stream_a = a.band_n ? 1 : 0;
+        a.stream_b = a.band_n ? 0 : 1;
+    } else {
+        a.band_n = 0;
+        a.band = static_cast<int32_t>(bal_m);
+    }
+    a.stream_d = p.rows * p.cols * 2 > 2 * L2_BAND_BYTES ? 1 : 0;
     const int work = a.tiles_m * a.tiles_n;
     const int grid = work < dev.sm_count ? work : dev.sm_count;
     kern<<<grid, NUM_THREADS, L::TOTAL, stream>>>(ta, tb, td, a);

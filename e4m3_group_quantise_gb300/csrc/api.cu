@@ -276,7 +276,11 @@ JETFP8_API jetfp8_status jetfp8_quantize_weight(const void *w, int64_t N, int64_
     jetfp8_status st = current_device(&dev);
     if (st != JETFP8_OK)
         return st;
-    return launch_status(jetfp8::launch_quantize_weight(w, N, K, q, s, qt, static_cast<cudaStream_t>(stream)));
+    std::call_once(g_encode_once, init_encode);
+    if (g_encode == nullptr)
+        return JETFP8_ERR_UNSUPPORTED_DEVICE;
+    return launch_status(jetfp8::launch_quantize_weight(w, N, K, q, s, qt, g_encode, dev->err_word, dev->sm_count,
+                                                        static_cast<cudaStream_t>(stream)));
 }
 
 JETFP8_API jetfp8_status jetfp8_rmsnorm_quantize_act(const void *x, const void *gamma, float eps, int64_t M,

@@ -17,7 +17,7 @@ enum : uint32_t {
     ERRBIT_PROMOTE = 1u << 3,    // promotion warps: waiting for a finished TMEM partial
     ERRBIT_DRAIN = 1u << 4,      // teardown: waiting for copies / MMAs in flight
     ERRBIT_SELFTEST = 1u << 5,   // the watchdog self-test kernel
-    ERRBIT_QUANT = 1u << 6,      // dual quantiser: waiting for its tile
+    ERRBIT_QUANT = 1u << 6,      // dual / weight quantiser: waiting for its tile
 };
 
 // Quantisers (quantize.cu).  All return the cudaGetLastError() of the launch.
@@ -29,6 +29,7 @@ cudaError_t launch_quantize_act_dual(const void *x, int64_t M, int64_t K, uint8_
                                      float *st, PFN_cuTensorMapEncodeTiled_v12000 encode, uint32_t *err,
                                      cudaStream_t stream);
 cudaError_t launch_quantize_weight(const void *w, int64_t N, int64_t K, uint8_t *q, float *s, uint8_t *qt,
+                                   PFN_cuTensorMapEncodeTiled_v12000 encode, uint32_t *err, int sm_count,
                                    cudaStream_t stream);
 cudaError_t launch_e4m3_encode_range(uint32_t first, int64_t count, uint8_t *codes, int sm_count,
                                      cudaStream_t stream);

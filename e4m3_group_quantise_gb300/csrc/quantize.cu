@@ -34,6 +34,21 @@ namespace {
 // lanes with sub == 0 store them as one 32-byte sector -- no shared memory.
 // The amax needs two shuffles; the scale arithmetic is shared by 32 values.
 // ---------------------------------------------------------------------------
+// Four bf16 values (word k, k = 0..7) of a lane's 32 held as four 16-byte
+// chunks: chunk k / 2, half k % 2; picked by selects, so the rare exact path
+// needs neither a memory access nor an indexed register array.
+__device__ __forceinline__ uint2 pick_word(const uint4 (&v)[4], int k)
+{
+    uint2 r = make_uint2(v[0].x, v[0].y);
+#pragma unroll
+    for (int i = 1; i < 8; ++i) {
+        const uint4 &c = v[i >> 1];
+        const uint2 cand = (i & 1) ? make_uint2(c.z, c.w) : make_uint2(c.x, c.y);
+        r = (k == i) ? cand : r;
+    }
+    return r;
+}
+
 constexpr int Q1_ROWS = 16;
 constexpr int Q1_GROUPS = 8;
 constexpr int Q1_THREADS = 256;
@@ -183,99 +198,190 @@ quantize_act_t_kernel(const uint4 *__restrict__ x, int64_t M, int64_t C, uint8_t
 }
 
 // ---------------------------------------------------------------------------
-// 128x128 weight blocks.  One CTA per block: 16 lanes cover a 128-wide row,
-// 16 rows per pass, 8 passes; amax through warp shuffles and a shared-memory
-// combine of the 8 warps.  With `qt` the codes are also staged in shared
-// memory and written transposed (each thread: 16 codes of four output rows).
+// 128x128 weight blocks.  Persistent CTAs (two per SM) walk the blocks in
+// row-major order, block b, b + gridDim.x, ...; each block arrives by two
+// bulk tensor copies (TMA, 128-byte swizzle, as in the dual quantiser) into
+// one of two shared-memory stages, so the next block is in flight while this
+// one is encoded.  Per block (8 warps):
+//   read:      warp w takes rows 16w .. 16w+15, eight rows per step, four
+//              lanes per row holding 32 values each (16-byte chunks sub,
+//              sub+4, sub+8, sub+12), kept in registers as bf16 words;
+//   amax:      lane maxima, warp shuffles, one value per warp in shared
+//              memory, one barrier -- after which the stage is free and the
+//              block two ahead is requested into it;
+//   encode:    the codes of the lane's 32 values with the block's scale,
+//              written to q (32 contiguous bytes per row quarter) and to a
+//              shared code tile;
+//   transpose: after a barrier, each lane reads four code columns of 16 rows
+//              from the tile and writes them, transposed by byte permutes,
+//              as 16-byte runs of qt's rows; the two lanes of a pair take
+//              adjacent 16-row ranges, so each store instruction writes whole
+//              32-byte sectors.
+// The next block's first barrier orders this block's tile reads before the
+// next block's tile writes.
 // ---------------------------------------------------------------------------
-constexpr int Q3_THREADS = 256;
+constexpr int QW_THREADS = 256;
+constexpr int QW_STAGES = 2;
+constexpr int QW_CODE_PITCH = 160;           // bytes per code-tile row: row-pass writes in two wavefronts
 
-__global__ void __launch_bounds__(Q3_THREADS)
-quantize_weight_kernel(const uint4 *__restrict__ w, int64_t N, int64_t K, uint2 *__restrict__ q,
-                       float *__restrict__ s, uint8_t *__restrict__ qt)
+struct WeightSmem {
+    uint8_t tile[QW_STAGES][2][128][128];    // per stage: two 64-column halves, 128-byte swizzle
+    uint8_t codes[128][QW_CODE_PITCH];
+    uint64_t full[QW_STAGES];
+    float red[QW_THREADS / 32];
+};
+constexpr uint32_t QW_SMEM_BYTES = sizeof(WeightSmem) + 1024;   // + alignment slack
+
+__device__ __forceinline__ const uint8_t *weight_chunk(const WeightSmem &sm, int stage, int r, int c)
 {
-    __shared__ float s_red[Q3_THREADS / 32];
-    __shared__ __align__(16) uint8_t s_codes[128][128];
-    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-    const int sub = t & 15, r0 = t >> 4;
-    const int64_t bk = blockIdx.x, bn = blockIdx.y;
-    const int64_t K8 = K >> 3;
+    return &sm.tile[stage][c >> 3][r][((c & 7) ^ (r & 7)) << 4];
+}
 
-    uint4 v[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-        v[i] = __ldcs(w + (bn * 128 + r0 + 16 * i) * K8 + bk * 16 + sub);
 
-    float amax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        float f[8];
-        unpack8(v[i], f);
-        amax = fmaxf(amax, absmax8(f));
+
+__global__ void __launch_bounds__(QW_THREADS, 2)
+quantize_weight_kernel(const __grid_constant__ CUtensorMap tmap_w, int64_t N, int64_t K, uint8_t *__restrict__ q,
+                       float *__restrict__ s, uint8_t *__restrict__ qt, uint32_t *__restrict__ err)
+{
+    extern __shared__ uint8_t weight_smem_raw[];
+    WeightSmem &sm = *reinterpret_cast<WeightSmem *>((reinterpret_cast<uintptr_t>(weight_smem_raw) + 1023) &
+                                                     ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t bk_count = K >> 7;
+    const int64_t blocks = (N >> 7) * bk_count;
+    const int64_t first = blockIdx.x, stride = gridDim.x;
+    constexpr uint32_t TILE_BYTES = 128 * 128 * 2;
+
+    auto request = [&](int64_t blk, int stage) {   // one thread: bring block blk into stage
+        const int32_t n0 = static_cast<int32_t>((blk / bk_count) << 7), k0 = static_cast<int32_t>((blk % bk_count) << 7);
+        ptx::mbar_arrive_expect_tx(&sm.full[stage], TILE_BYTES);
+        ptx::tma_load_2d(&sm.tile[stage][0][0][0], &tmap_w, &sm.full[stage], k0, n0);
+        ptx::tma_load_2d(&sm.tile[stage][1][0][0], &tmap_w, &sm.full[stage], k0 + 64, n0);
+    };
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < QW_STAGES; ++st)
+            ptx::mbar_init(&sm.full[st], 1);
+        ptx::fence_mbar_init();
+        ptx::tma_prefetch_desc(&tmap_w);
+        for (int st = 0; st < QW_STAGES; ++st)
+            if (first + st * stride < blocks)
+                request(first + st * stride, st);
     }
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1)
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    if (lane == 0)
-        s_red[warp] = amax;
     __syncthreads();
-    amax = s_red[0];
-#pragma unroll
-    for (int i = 1; i < Q3_THREADS / 32; ++i)
-        amax = fmaxf(amax, s_red[i]);
-    const GroupScale gs = group_scale(amax);
-    if (t == 0)
-        s[bn * (K >> 7) + bk] = gs.s;
 
-    uint32_t redo = 0u;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        float f[8];
-        unpack8(v[i], f);
-        uint32_t wd[2];
-        redo |= encode_words<2>(f, gs, wd) << (2 * i);
-        const uint2 codes = make_uint2(wd[0], wd[1]);
-        const int r = r0 + 16 * i;
-        __stcs(q + (bn * 128 + r) * K8 + bk * 16 + sub, codes);
-        if (qt != nullptr)
-            *reinterpret_cast<uint2 *>(&s_codes[r][sub * 8]) = codes;
-    }
-    // rare: words whose bracket disagreed get the exact quotient
-    while (redo != 0u) {
-        const int b = __ffs(redo) - 1;
-        redo &= redo - 1u;
-        const int r = r0 + 16 * (b >> 1), c = sub * 8 + 4 * (b & 1);
-        const int64_t e = (bn * 128 + r) * K + bk * 128 + c;
-        const uint32_t code =
-            encode4_exact(*reinterpret_cast<const uint2 *>(reinterpret_cast<const uint16_t *>(w) + e), gs.s);
-        *reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(q) + e) = code;
-        if (qt != nullptr)
-            *reinterpret_cast<uint32_t *>(&s_codes[r][c]) = code;
-    }
-    if (qt == nullptr)
-        return;
-    __syncthreads();
-    // transposed write: lane l of warp w takes output rows 4l .. 4l+3 (columns
-    // of the block) and their codes for block rows 16w .. 16w+15: sixteen
-    // 4-byte reads (one block row each, conflict-free across the warp), a
-    // 4 x 4 byte transpose per four rows, one 16-byte store per output row
-    const int kq = 4 * lane, n0 = 16 * warp;
-    uint32_t rw[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-        rw[i] = *reinterpret_cast<const uint32_t *>(&s_codes[n0 + i][kq]);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        uint32_t o[4];
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            // byte j of block rows 4b .. 4b+3: the codes of column kq + j
-            const uint32_t lo = __byte_perm(rw[4 * b], rw[4 * b + 1], j | ((4 + j) << 4));
-            const uint32_t hi = __byte_perm(rw[4 * b + 2], rw[4 * b + 3], j | ((4 + j) << 4));
-            o[b] = __byte_perm(lo, hi, 0x5410);
+    const int rr = lane >> 2, sub = lane & 3;
+    int it = 0;
+    for (int64_t blk = first; blk < blocks; blk += stride, ++it) {
+        const int stage = it % QW_STAGES;
+        const uint32_t phase = static_cast<uint32_t>(it / QW_STAGES) & 1u;
+        const bool landed = ptx::mbar_wait(&sm.full[stage], phase, nullptr, err, ERRBIT_QUANT, 2000000000ull);
+        if (__syncthreads_or(!landed)) {
+            // give up together; the copies still requested must land before exit
+            if (threadIdx.x == 0)
+                for (int k = 0; k < QW_STAGES; ++k) {
+                    const int64_t b2 = blk + k * stride;
+                    if (b2 < blocks)
+                        ptx::mbar_wait(&sm.full[(it + k) % QW_STAGES], static_cast<uint32_t>((it + k) / QW_STAGES) & 1u,
+                                       nullptr, err, ERRBIT_DRAIN, 2000000000ull);
+                }
+            return;
         }
-        __stcs(reinterpret_cast<uint4 *>(qt + (bk * 128 + kq + j) * N + bn * 128 + n0),
-               make_uint4(o[0], o[1], o[2], o[3]));
+        const int64_t n_base = (blk / bk_count) << 7, k_base = (blk % bk_count) << 7;
+
+        // ---- read this lane's 64 values and their amax
+        uint4 v[2][4];
+        float amax = 0.0f;
+#pragma unroll
+        for (int step = 0; step < 2; ++step) {
+            const int r = 16 * warp + 8 * step + rr;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                v[step][j] = *reinterpret_cast<const uint4 *>(weight_chunk(sm, stage, r, sub + 4 * j));
+                float f[8];
+                unpack8(v[step][j], f);
+                amax = fmaxf(amax, absmax8(f));
+            }
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1)
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        if (lane == 0)
+            sm.red[warp] = amax;
+        __syncthreads();   // every read of this stage is done; the block's warp maxima are visible
+        if (threadIdx.x == 0 && blk + QW_STAGES * stride < blocks)
+            request(blk + QW_STAGES * stride, stage);
+        amax = sm.red[0];
+#pragma unroll
+        for (int i = 1; i < QW_THREADS / 32; ++i)
+            amax = fmaxf(amax, sm.red[i]);
+        const GroupScale gs = group_scale(amax);
+        if (threadIdx.x == 0)
+            s[(n_base >> 7) * bk_count + (k_base >> 7)] = gs.s;
+
+        // ---- encode: codes to q and to the shared code tile
+#pragma unroll
+        for (int step = 0; step < 2; ++step) {
+            const int r = 16 * warp + 8 * step + rr;
+            float f[32];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float u[8];
+                unpack8(v[step][j], u);
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    f[8 * j + e] = u[e];
+            }
+            uint32_t wd[8];
+            uint32_t redo = encode_words<8>(f, gs, wd);
+            uint8_t *row_q = q + (n_base + r) * K + k_base;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint2 c = make_uint2(wd[2 * j], wd[2 * j + 1]);
+                __stcs(reinterpret_cast<uint2 *>(row_q + 8 * (sub + 4 * j)), c);
+                if (qt != nullptr)
+                    *reinterpret_cast<uint2 *>(&sm.codes[r][8 * (sub + 4 * j)]) = c;
+            }
+            // rare: a word whose bracket disagreed gets the exact quotient, its
+            // four inputs taken from the lane's registers (word k: chunk
+            // sub + 4(k/2), half k%2)
+            while (redo != 0u) {
+                const int k = __ffs(redo) - 1;
+                redo &= redo - 1u;
+                const int col = 8 * (sub + 4 * (k >> 1)) + 4 * (k & 1);
+                const uint32_t code = encode4_exact(pick_word(v[step], k), gs.s);
+                *reinterpret_cast<uint32_t *>(row_q + col) = code;
+                if (qt != nullptr)
+                    *reinterpret_cast<uint32_t *>(&sm.codes[r][col]) = code;
+            }
+        }
+        if (qt == nullptr)
+            continue;
+        __syncthreads();   // the code tile is complete
+
+        // ---- transposed write: lane l of warp w takes output rows kq .. kq+3
+        // (columns of the block, kq = 64 (w / 4) + 4 (l / 2)) and their codes
+        // for block rows n0 .. n0+15 (n0 = 32 (w % 4) + 16 (l % 2)): sixteen
+        // 4-byte reads (one block row each), a 4 x 4 byte transpose per four
+        // rows, one 16-byte store per output row, lanes 2i and 2i+1 filling
+        // the two halves of one 32-byte sector
+        const int kq = 64 * (warp >> 2) + 4 * (lane >> 1), n0 = 32 * (warp & 3) + 16 * (lane & 1);
+        uint32_t rw[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            rw[i] = *reinterpret_cast<const uint32_t *>(&sm.codes[n0 + i][kq]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint32_t o[4];
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                // byte j of block rows 4b .. 4b+3: the codes of column kq + j
+                const uint32_t lo = __byte_perm(rw[4 * b], rw[4 * b + 1], j | ((4 + j) << 4));
+                const uint32_t hi = __byte_perm(rw[4 * b + 2], rw[4 * b + 3], j | ((4 + j) << 4));
+                o[b] = __byte_perm(lo, hi, 0x5410);
+            }
+            __stcs(reinterpret_cast<uint4 *>(qt + (k_base + kq + j) * N + n_base + n0),
+                   make_uint4(o[0], o[1], o[2], o[3]));
+        }
     }
 }
 
@@ -300,7 +406,9 @@ quantize_weight_kernel(const uint4 *__restrict__ w, int64_t N, int64_t K, uint2 
 //            group is four lanes of one warp (amax: two shuffles).  The tile is
 //            read-only once it has landed, so no barrier separates the passes.
 //            The interleaved codes are put back in row order through a small
-//            per-warp staging buffer and leave as two 16-byte stores per lane.
+//            per-warp staging buffer and leave as two 16-byte stores per lane,
+//            arranged so that each store instruction writes whole 32-byte
+//            sectors.
 // ---------------------------------------------------------------------------
 constexpr int QD_TILE = 128;
 constexpr int QD_THREADS = 256;
@@ -472,13 +580,20 @@ quantize_act_dual_kernel(const __grid_constant__ CUtensorMap tmap_x, int64_t M, 
             }
         }
         __syncwarp();
-        // lane 4c + q now takes rows 32q .. 32q+31 of column c: two 16-byte stores
-        const uint8_t *src = stg + cc * QD_STAGE_PITCH + 32 * cq;
-        const uint32_t *s32 = reinterpret_cast<const uint32_t *>(src);
+        // Column c's 128 codes leave as four 32-byte sectors (rows 32t .. 32t+31,
+        // t = 0..3), each written whole by one store instruction: lanes 4c + q
+        // with q = 2p and 2p+1 write the two 16-byte halves of sector 2p, then of
+        // sector 2p+1 (a sector written in two halves by two instructions costs
+        // DRAM bandwidth)
         const int64_t colg = k0 + 8 * chunk + cc;
-        uint4 *dst = reinterpret_cast<uint4 *>(qt + colg * M + m0 + 32 * cq);
-        __stcs(dst, make_uint4(s32[0], s32[1], s32[2], s32[3]));
-        __stcs(dst + 1, make_uint4(s32[4], s32[5], s32[6], s32[7]));
+        const int pair = cq >> 1, half = cq & 1;
+#pragma unroll
+        for (int t2 = 0; t2 < 2; ++t2) {
+            const int sector = 2 * pair + t2;
+            const uint32_t *s32 = reinterpret_cast<const uint32_t *>(stg + cc * QD_STAGE_PITCH + 32 * sector + 16 * half);
+            __stcs(reinterpret_cast<uint4 *>(qt + colg * M + m0 + 32 * sector + 16 * half),
+                   make_uint4(s32[0], s32[1], s32[2], s32[3]));
+        }
         if (cq == 0)
             st[(m0 >> 7) * K + colg] = gs.s;
         __syncwarp();                                 // the staging buffer is reused next pass
@@ -505,14 +620,6 @@ cudaError_t launch_quantize_act_transposed(const void *x, int64_t M, int64_t C, 
     return cudaGetLastError();
 }
 
-cudaError_t launch_quantize_weight(const void *w, int64_t N, int64_t K, uint8_t *q, float *s, uint8_t *qt,
-                                   cudaStream_t stream)
-{
-    dim3 grid(static_cast<unsigned>(K / 128), static_cast<unsigned>(N / 128));
-    quantize_weight_kernel<<<grid, Q3_THREADS, 0, stream>>>(static_cast<const uint4 *>(w), N, K,
-                                                            reinterpret_cast<uint2 *>(q), s, qt);
-    return cudaGetLastError();
-}
 
 namespace {
 // codes[i] = E4M3 code of the fp32 pattern first + i, through the same
@@ -557,6 +664,31 @@ cudaError_t launch_e4m3_encode_range(uint32_t first, int64_t count, uint8_t *cod
 }  // namespace jetfp8
 
 namespace jetfp8 {
+cudaError_t launch_quantize_weight(const void *w, int64_t N, int64_t K, uint8_t *q, float *s, uint8_t *qt,
+                                   PFN_cuTensorMapEncodeTiled_v12000 encode, uint32_t *err, int sm_count,
+                                   cudaStream_t stream)
+{
+    // W [N][K] bf16 seen as 128-row x 64-column boxes with the 128-byte swizzle
+    CUtensorMap tmap;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+    cuuint32_t box[2] = {64, 128};
+    cuuint32_t estr[2] = {1, 1};
+    if (encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(w), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(quantize_weight_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(QW_SMEM_BYTES));
+    if (e != cudaSuccess)
+        return e;
+    const int64_t blocks = (N / 128) * (K / 128);
+    const int64_t cap = static_cast<int64_t>(sm_count) * 2;   // two resident CTAs per SM
+    const unsigned grid = static_cast<unsigned>(blocks < cap ? blocks : cap);
+    quantize_weight_kernel<<<grid, QW_THREADS, QW_SMEM_BYTES, stream>>>(tmap, N, K, q, s, qt, err);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_quantize_act_dual(const void *x, int64_t M, int64_t K, uint8_t *q, float *s, uint8_t *qt,
                                      float *st, PFN_cuTensorMapEncodeTiled_v12000 encode, uint32_t *err,
                                      cudaStream_t stream)

@@ -450,8 +450,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                 if (!SB_PER_COLUMN) {
                     w_blk = scur[row_in_tile] * scur[BM + (wg * COLS_PER_WG) / 128];
                     __syncwarp();
-                    if (lane == 0)
-                        ptx::mbar_arrive(&sempty[ss]);
+                    ptx::mbar_arrive_elected(&sempty[ss]);
                 }
 
                 if (!ptx::mbar_wait(&tfull[buf], bphase, abort_flag, args.err, ERRBIT_PROMOTE, WAIT_TIMEOUT_NS)) {
@@ -459,8 +458,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                     break;
                 }
                 ptx::tc_fence_after();
-                if (warp == FIRST_PROMO_WARP && lane == 0)
-                    ptx::mbar_arrive(&empty[it % STAGES]);      // the group's MMAs are done with it
+                if (warp == FIRST_PROMO_WARP) {                  // the group's MMAs are done with it
+                    if (SB_PER_COLUMN) {
+                        if (lane == 0)
+                            ptx::mbar_arrive(&empty[it % STAGES]);
+                    } else {
+                        ptx::mbar_arrive_elected(&empty[it % STAGES]);
+                    }
+                }
                 const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + buf * BN +
                                        wg * COLS_PER_WG;
                 if (SB_PER_COLUMN) {
@@ -490,8 +495,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                             // the whole partial is in registers: hand the buffer back
                             ptx::tc_fence_before();
                             __syncwarp();
-                            if (lane == 0)
-                                ptx::mbar_arrive(&tempty[buf]);
+                            ptx::mbar_arrive_elected(&tempty[buf]);
                         }
 #pragma unroll
                         for (int i = 0; i < PS; ++i) {
@@ -528,8 +532,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                                 // the whole partial is in registers: hand the buffer back
                                 ptx::tc_fence_before();
                                 __syncwarp();
-                                if (lane == 0)
-                                    ptx::mbar_arrive(&tempty[buf]);
+                                ptx::mbar_arrive_elected(&tempty[buf]);
                             }
                             apply32(*reinterpret_cast<const uint32_t(*)[32]>(pp), h * 64);
                             apply32(*reinterpret_cast<const uint32_t(*)[32]>(pp + 32), h * 64 + 32);
@@ -540,15 +543,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                         ptx::tmem_ld_wait(p0);
                         ptx::tc_fence_before();
                         __syncwarp();
-                        if (lane == 0)
-                            ptx::mbar_arrive(&tempty[buf]);
+                        ptx::mbar_arrive_elected(&tempty[buf]);
                         apply32(p0, 0);
                     }
                 }
                 if (SB_PER_COLUMN) {
                     __syncwarp();
-                    if (lane == 0)
-                        ptx::mbar_arrive(&sempty[ss]);
+                    ptx::mbar_arrive_elected(&sempty[ss]);
                 }
                 if (++ss == SCALE_STAGES) {
                     ss = 0;

@@ -45,6 +45,17 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// Arrive once on `bar` from one lane of the (converged) warp, chosen by
+// elect.sync; the other lanes skip it by predicate, without a branch.
+__device__ __forceinline__ void mbar_arrive_elected(uint64_t *bar)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "@p mbarrier.arrive.shared::cta.b64 _, [%0];\n\t}" ::"r"(smem_u32(bar))
+        : "memory");
+}
+
 // One potentially blocking test of the phase with parity `parity`: the thread
 // is suspended (issuing nothing) until the phase completes or about
 // `suspend_ns` nanoseconds pass, whichever is first.

@@ -119,8 +119,9 @@ quantize_act_kernel(const uint4 *__restrict__ x, int64_t M, int64_t K, uint2 *__
 // per row).  Warp q takes rows 32q .. 32q+31; lane l takes the column pair
 // 2l, 2l+1, reading one 4-byte word per row (a warp reads one contiguous
 // 128-byte row per step: no bank conflicts).  The four row quarters combine
-// their amax through shared memory; each thread then writes 32 contiguous
-// codes (one 32-byte sector) to each of its two output rows.
+// their amax through shared memory; each column's 32 codes of a quarter
+// (one 32-byte sector of an output row) then leave whole, two lanes per
+// sector per store instruction.
 // ---------------------------------------------------------------------------
 constexpr int Q2_ROWS = 128;
 constexpr int Q2_COLS = 64;
@@ -172,16 +173,11 @@ quantize_act_t_kernel(const uint4 *__restrict__ x, int64_t M, int64_t C, uint8_t
     uint32_t w0[8], w1[8];
     uint32_t redo = encode_words<8>(f0, g0, w0) | (encode_words<8>(f1, g1, w1) << 8);
     const int64_t col = c0 + 2 * lane;
-    uint4 *d0 = reinterpret_cast<uint4 *>(qt + col * M + m0 + 32 * q);
-    uint4 *d1 = reinterpret_cast<uint4 *>(qt + (col + 1) * M + m0 + 32 * q);
-    __stcs(d0, make_uint4(w0[0], w0[1], w0[2], w0[3]));
-    __stcs(d0 + 1, make_uint4(w0[4], w0[5], w0[6], w0[7]));
-    __stcs(d1, make_uint4(w1[0], w1[1], w1[2], w1[3]));
-    __stcs(d1 + 1, make_uint4(w1[4], w1[5], w1[6], w1[7]));
     if (q == 0)
         *reinterpret_cast<float2 *>(st + (m0 >> 7) * C + col) = make_float2(g0.s, g1.s);
     // rare: words whose bracket disagreed get the exact quotient (inputs re-read
-    // from the shared-memory tile: 4 rows of this thread's column)
+    // from the shared-memory tile: 4 rows of this thread's column), patched in
+    // the registers before anything is stored
     while (redo != 0u) {
         const int b = __ffs(redo) - 1;
         redo &= redo - 1u;
@@ -192,9 +188,39 @@ quantize_act_t_kernel(const uint4 *__restrict__ x, int64_t M, int64_t C, uint8_t
             const uint32_t wv = reinterpret_cast<const uint32_t *>(&tile[32 * q + 4 * k + e][0])[lane];
             v4[e] = hi ? bf16_hi(wv) : bf16_lo(wv);
         }
-        *reinterpret_cast<uint32_t *>(qt + (col + hi) * M + m0 + 32 * q + 4 * k) =
-            encode4_exact(v4[0], v4[1], v4[2], v4[3], hi ? g1.s : g0.s);
+        const uint32_t fixed = encode4_exact(v4[0], v4[1], v4[2], v4[3], hi ? g1.s : g0.s);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            w0[i] = (!hi && k == i) ? fixed : w0[i];
+            w1[i] = (hi && k == i) ? fixed : w1[i];
+        }
     }
+    // Each column's 32 codes of this row quarter form one 32-byte sector.  Lane
+    // pairs (2i, 2i+1) exchange halves so that every store instruction writes
+    // whole sectors: the even lane writes bytes 0-15 and the odd lane bytes
+    // 16-31 of the same column (a sector written in two halves by two
+    // instructions costs DRAM bandwidth).  The even lane holds columns
+    // c, c+1 and the odd lane c+2, c+3 (c = c0 + 4i).
+    const bool odd = lane & 1;
+    uint32_t x0[4], x1[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        x0[k] = __shfl_xor_sync(0xffffffffu, odd ? w0[k] : w0[4 + k], 1);
+        x1[k] = __shfl_xor_sync(0xffffffffu, odd ? w1[k] : w1[4 + k], 1);
+    }
+    const int64_t cp = c0 + 2 * (lane & ~1);          // the pair's first column
+    uint8_t *base = qt + m0 + 32 * q + (odd ? 16 : 0);
+    // column cp (the even lane's first): even its own bytes 0-15, odd the received 16-31
+    __stcs(reinterpret_cast<uint4 *>(base + cp * M),
+           odd ? make_uint4(x0[0], x0[1], x0[2], x0[3]) : make_uint4(w0[0], w0[1], w0[2], w0[3]));
+    // column cp + 2 (the odd lane's first)
+    __stcs(reinterpret_cast<uint4 *>(base + (cp + 2) * M),
+           odd ? make_uint4(w0[4], w0[5], w0[6], w0[7]) : make_uint4(x0[0], x0[1], x0[2], x0[3]));
+    // columns cp + 1 and cp + 3 (the lanes' second columns)
+    __stcs(reinterpret_cast<uint4 *>(base + (cp + 1) * M),
+           odd ? make_uint4(x1[0], x1[1], x1[2], x1[3]) : make_uint4(w1[0], w1[1], w1[2], w1[3]));
+    __stcs(reinterpret_cast<uint4 *>(base + (cp + 3) * M),
+           odd ? make_uint4(w1[4], w1[5], w1[6], w1[7]) : make_uint4(x1[0], x1[1], x1[2], x1[3]));
 }
 
 // ---------------------------------------------------------------------------

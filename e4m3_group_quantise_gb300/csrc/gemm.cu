@@ -100,12 +100,22 @@ struct KernelArgs {
     int32_t stream_d;     // 1: the output is larger than L2 can keep: store it with evict-first
 };
 
-template <int BN, int STAGES>
+// HALF_A (problems of at most 64 rows, i.e. decode): A arrives as a 64-row box
+// (no out-of-bounds fill for the missing rows) and consecutive stages' A
+// tiles are packed 64 rows (8 KB) apart.  The MMA still reads a 128-row
+// window: its rows 64..127 are the next stage's rows 0..63 (or the padding
+// after the last stage), which only feed output rows 64..127 -- rows past the
+// problem, never stored.  Halving A's footprint buys more stages, i.e. more of
+// W in flight, which is what bounds decode.
+template <int BN, int STAGES, bool HALF_A = false>
 struct Smem {
-    static constexpr uint32_t A_BYTES = BM * BK;
+    static constexpr uint32_t A_BYTES = HALF_A ? (BM / 2) * BK : BM * BK;   // A stride between stages
+    static constexpr uint32_t A_LOAD_BYTES = A_BYTES;                       // bytes one stage's A copy brings
+    static constexpr uint32_t A_PAD = HALF_A ? (BM / 2) * BK : 0;          // the last stage's window tail
     static constexpr uint32_t B_BYTES = BN * BK;
-    static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr uint32_t TILES = STAGES * STAGE_BYTES;
+    static constexpr uint32_t STAGE_BYTES = A_LOAD_BYTES + B_BYTES;
+    static constexpr uint32_t B_OFF = STAGES * A_BYTES + A_PAD;
+    static constexpr uint32_t TILES = B_OFF + STAGES * B_BYTES;
     // scale ring: per slot 128 row scales then BN column scales (fp32)
     static constexpr uint32_t SCALE_FLOATS = BM + BN;
     static constexpr uint32_t SCALE_OFF = TILES;
@@ -152,12 +162,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 __device__ __forceinline__ void tmem_ld_quads(uint32_t taddr, uint32_t (&r)[32]) { ptx::tmem_ld_16x256b_x8(taddr, r); }
 __device__ __forceinline__ void tmem_ld_quads(uint32_t taddr, uint32_t (&r)[16]) { ptx::tmem_ld_16x256b_x4(taddr, r); }
 
-template <int BN, int STAGES, bool SB_PER_COLUMN>
+template <int BN, int STAGES, bool SB_PER_COLUMN, bool HALF_A>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
             const __grid_constant__ CUtensorMap tmap_d, const KernelArgs args)
 {
-    using L = Smem<BN, STAGES>;
+    using L = Smem<BN, STAGES, HALF_A>;
     constexpr int SCALE_STAGES = L::SCALE_STAGES;
     // Tiles 128 or 256 wide: two promotion warpgroups, one per column half.
     // Narrow tiles (decode-sized problems): the first warpgroup alone.
@@ -201,7 +211,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sA = smem;
-    uint8_t *sB = smem + STAGES * L::A_BYTES;
+    uint8_t *sB = smem + L::B_OFF;
     float *scl = reinterpret_cast<float *>(smem + L::SCALE_OFF);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::BAR_OFF);
     uint64_t *empty = full + STAGES;
@@ -618,13 +628,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         ptx::tmem_dealloc(tmem_base, TMEM_COLS);
 }
 
-template <int BN, int STAGES, bool SB_PER_COLUMN>
+template <int BN, int STAGES, bool SB_PER_COLUMN, bool HALF_A = false>
 cudaError_t launch_variant(const GemmProblem &p, const DeviceInfo &dev, const CUtensorMap &ta, const CUtensorMap &tb,
                            const CUtensorMap &td, cudaStream_t stream)
 {
-    using L = Smem<BN, STAGES>;
+    using L = Smem<BN, STAGES, HALF_A>;
     static_assert(L::TOTAL <= 227 * 1024, "shared memory per CTA");
-    auto kern = gemm_kernel<BN, STAGES, SB_PER_COLUMN>;
+    static_assert(!HALF_A || !SB_PER_COLUMN, "the packed A tiles serve block-scale problems of <= 64 rows");
+    auto kern = gemm_kernel<BN, STAGES, SB_PER_COLUMN, HALF_A>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(L::TOTAL));
     if (e != cudaSuccess)
         return e;
@@ -732,12 +743,21 @@ cudaError_t launch_gemm(const GemmProblem &p, const DeviceInfo &dev, PFN_cuTenso
             bn = w;
         }
     }
+    const bool per_col = p.sb_mode == ScaleB::PerColumn;
+    const bool half_a = !per_col && p.rows <= BM / 2;   // decode: A fits a 64-row box
     CUtensorMap ta, tb, td;
-    if (encode_operand(encode, &ta, p.a, p.rows, p.kdim, BM) != CUDA_SUCCESS ||
+    if (encode_operand(encode, &ta, p.a, p.rows, p.kdim, half_a ? BM / 2 : BM) != CUDA_SUCCESS ||
         encode_operand(encode, &tb, p.b, p.cols, p.kdim, bn) != CUDA_SUCCESS ||
         encode_output(encode, &td, p.d, p.rows, p.cols) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
-    const bool per_col = p.sb_mode == ScaleB::PerColumn;
+    if (half_a) {
+        switch (bn) {
+        case 256: return launch_variant<256, 4, false, true>(p, dev, ta, tb, td, stream);
+        case 128: return launch_variant<128, 8, false, true>(p, dev, ta, tb, td, stream);
+        case 64: return launch_variant<64, 12, false, true>(p, dev, ta, tb, td, stream);
+        default: return launch_variant<32, 16, false, true>(p, dev, ta, tb, td, stream);
+        }
+    }
     switch (bn) {
     case 256:
         return per_col ? launch_variant<256, 4, true>(p, dev, ta, tb, td, stream)

@@ -98,6 +98,7 @@ struct KernelArgs {
     int32_t stream_a;     // 1: A's tiles are read once, load them with the evict-first L2 priority
     int32_t stream_b;     // 1: the same for B
     int32_t stream_d;     // 1: the output is larger than L2 can keep: store it with evict-first
+    uint32_t stage_bytes; // bytes one pipeline stage's two copies bring (A's box may be short)
 };
 
 // HALF_A (problems of at most 64 rows, i.e. decode): A arrives as a 64-row box
@@ -262,6 +263,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
+    // Programmatic dependent launch: the set-up above (barriers, TMEM, tensor
+    // map prefetch) may overlap the previous kernel of the stream; no global
+    // memory is read or written before that kernel has completed and its
+    // writes are visible.  Then the next kernel may begin its own set-up.
+    ptx::grid_dependency_wait();
+    ptx::launch_dependents();
     const uint32_t tmem_base = *tmem_holder;
 
     if (warp < FIRST_PROMO_WARP) {
@@ -308,7 +315,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                             ok = false;
                             break;
                         }
-                        ptx::mbar_arrive_expect_tx(&full[stage], L::STAGE_BYTES);
+                        ptx::mbar_arrive_expect_tx(&full[stage], args.stage_bytes);
                         ptx::tma_load_2d_hint(sA + stage * L::A_BYTES, &tmap_a, &full[stage], g * BK, tm * BM, pol_a);
                         ptx::tma_load_2d_hint(sB + stage * L::B_BYTES, &tmap_b, &full[stage], g * BK, tn * BN, pol_b);
                         issued_mask |= 1u << stage;
@@ -628,6 +635,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         ptx::tmem_dealloc(tmem_base, TMEM_COLS);
 }
 
+// A's box height: a whole 128-row tile, or for a problem of fewer rows only the
+// rows present (rounded up to the 8-row swizzle atom), so that no copy is spent
+// on out-of-bounds fill.  The tile's rows beyond the box are never written by
+// the copy; they only feed output rows past the problem, which are not stored.
+int64_t a_box_rows(int64_t rows)
+{
+    return rows >= BM ? BM : ((rows + 7) / 8) * 8;
+}
+
 template <int BN, int STAGES, bool SB_PER_COLUMN, bool HALF_A = false>
 cudaError_t launch_variant(const GemmProblem &p, const DeviceInfo &dev, const CUtensorMap &ta, const CUtensorMap &tb,
                            const CUtensorMap &td, cudaStream_t stream)
@@ -689,9 +705,24 @@ cudaError_t launch_variant(const GemmProblem &p, const DeviceInfo &dev, const CU
         a.band = static_cast<int32_t>(bal_m);
     }
     a.stream_d = p.rows * p.cols * 2 > 2 * L2_BAND_BYTES ? 1 : 0;
+    a.stage_bytes = static_cast<uint32_t>(a_box_rows(p.rows)) * BK + L::B_BYTES;
     const int work = a.tiles_m * a.tiles_n;
     const int grid = work < dev.sm_count ? work : dev.sm_count;
-    kern<<<grid, NUM_THREADS, L::TOTAL, stream>>>(ta, tb, td, a);
+    // launched as a programmatic dependent of the stream's previous kernel
+    // (the kernel itself waits for it before touching global memory)
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = L::TOTAL;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, ta, tb, td, a);
+    if (e != cudaSuccess)
+        return e;
     return cudaGetLastError();
 }
 
@@ -746,7 +777,7 @@ cudaError_t launch_gemm(const GemmProblem &p, const DeviceInfo &dev, PFN_cuTenso
     const bool per_col = p.sb_mode == ScaleB::PerColumn;
     const bool half_a = !per_col && p.rows <= BM / 2;   // decode: A fits a 64-row box
     CUtensorMap ta, tb, td;
-    if (encode_operand(encode, &ta, p.a, p.rows, p.kdim, half_a ? BM / 2 : BM) != CUDA_SUCCESS ||
+    if (encode_operand(encode, &ta, p.a, p.rows, p.kdim, static_cast<int>(a_box_rows(p.rows))) != CUDA_SUCCESS ||
         encode_operand(encode, &tb, p.b, p.cols, p.kdim, bn) != CUDA_SUCCESS ||
         encode_output(encode, &td, p.d, p.rows, p.cols) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;

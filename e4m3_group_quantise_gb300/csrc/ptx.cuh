@@ -462,6 +462,21 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int m, int n)
            | (static_cast<uint32_t>(m >> 4) << 24);   // M / 16
 }
 
+// ------------------------------------------------------------ dependent launch
+// Wait until the grids this one depends on (the previous kernel of the stream,
+// when launched as a programmatic dependent) have completed and their memory
+// is visible; returns at once otherwise.
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Allow the next programmatic dependent kernel of the stream to be scheduled.
+__device__ __forceinline__ void launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------ registers
 // Per-warpgroup register rebalancing; all four warps of a warpgroup execute it.
 template <uint32_t N>

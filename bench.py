@@ -458,44 +458,55 @@ class L2Flush:
         torch.cuda._sleep(100_000)          # about 50 us of GPU clock cycles
 
 
-def time_decode(device, pk, iters: int = 20):
+def time_decode(device, pk, rounds: int = 8):
     """Config: rollout decode, Fprop alone at M = 64 and 256 on the four 8B
-    projections, L2 flushed before every launch.  The bound is HBM on W."""
+    projections, W read from HBM.  The launches run back to back over C
+    copies of the quantised weight (C x W at least three times the L2), so
+    each launch finds its W evicted by the others; one pair of CUDA events
+    brackets rounds x C launches (a per-launch event pair is too coarse for
+    10-40 us kernels).  The bound is HBM on W."""
     import e4m3_group_quantise_gb300 as jf
-    flush = L2Flush(device)
+    l2 = getattr(torch.cuda.get_device_properties(device), "L2_cache_size", 0) or (132 << 20)
     out = {}
     launches = 0
     for i, (name, (n, k)) in enumerate(syn.PROJ_8B.items()):
-        w = syn.weight(n, k, seed=2, index=i, device=device)
-        qw, sw, _ = jf.quantize_weight(w, transposed=False)
+        w_bytes = n * k + 4 * (n // 128) * (k // 128)
+        copies = max(4, -(-3 * l2 // w_bytes))
+        ws = []
+        for c in range(copies):
+            w = syn.weight(n, k, seed=2 + c, index=i, device=device)
+            ws.append(jf.quantize_weight(w, transposed=False)[:2])
+            del w
         for m in (64, 256):
             x = syn.activation(m, k, seed=3, index=i, device=device)
             qx, sx = jf.quantize_act(x)
             y = torch.empty(m, n, dtype=torch.bfloat16, device=device)
-            times = []
-            for it in range(iters + 3):
-                flush()
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record()
+            for qw, sw in ws:                       # warm-up: one pass over the copies
                 jf.jetfp8_gemm_fprop(qx, sx, qw, sw, y)
-                e1.record()
-                launches += 1
-                if it >= 3:
-                    times.append((e0, e1))
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(rounds):
+                for qw, sw in ws:
+                    jf.jetfp8_gemm_fprop(qx, sx, qw, sw, y)
+            e1.record()
             torch.cuda.synchronize()
             check_device(jf)
-            ms = float(np.median([a.elapsed_time(b) for a, b in times]))
-            w_bytes = n * k + 4 * (n // 128) * (k // 128)
+            launches += (rounds + 1) * copies
+            ms = e0.elapsed_time(e1) / (rounds * copies)
             all_bytes = w_bytes + m * k + 4 * m * (k // 128) + 2 * m * n
             out[f"{name}_m{m}"] = {"us": round(ms * 1e3, 2), "tflops": round(2.0 * m * n * k / (ms * 1e-3) / 1e12, 1),
                                    "w_gbs": round(w_bytes / (ms * 1e-3) / 1e9, 1),
                                    "w_frac_of_hbm": round(w_bytes / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 3),
-                                   "all_bytes_gbs": round(all_bytes / (ms * 1e-3) / 1e9, 1)}
+                                   "all_bytes_gbs": round(all_bytes / (ms * 1e-3) / 1e9, 1),
+                                   "weight_copies": copies}
+        del ws
+        torch.cuda.empty_cache()
     return {"config": "rollout decode: fprop at M=64 and M=256 on qkv 6144x4096, o 4096x4096, gate_up "
                       "28672x4096, down 4096x14336; X N(0,1), W N(0,0.02)",
-            "timing": f"median of {iters} launches, each between CUDA events after an L2 flush "
-                      "(a 2x-L2 buffer written) and a short spin that lets the host queue the launch, "
-                      "so W comes from HBM and the host's launch latency is not timed",
+            "timing": f"{rounds} rounds of back-to-back launches over C copies of the quantised weight (C x W "
+                      ">= 3 x L2, so each launch reads its W from HBM), one CUDA event pair per case; "
+                      "us per launch = elapsed / launches (includes the gap between back-to-back launches)",
             "bound": "hbm (W read)", "cases": out}, launches
 
 

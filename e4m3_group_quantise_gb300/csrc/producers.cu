@@ -8,17 +8,15 @@
 // and SwiGLU y = silu(g) * u, each bf16 result within one bf16 ulp of the
 // exact value (for gates below -87, where the fp32 sigmoid underflows, within
 // 2^-119 |u|; rows whose sum of squares overflows fp32 are outside the
-// domain).  The kernels evaluate them in fp32 in a fixed order (every
-// operation one IEEE fp32 operation, written with the _rn intrinsics and
-// fmaf so that nothing is contracted), so a row's result never depends on
-// the launch or on the other rows; the bf16 value (nearest even) is then
-// quantised exactly as jetfp8_quantize_act quantises it, and the optional
-// bf16 output is that same value.
+// domain).  The kernels evaluate them in fp32 in a fixed order, so a
+// row's result never depends on the launch or on the other rows; the bf16
+// value (nearest even) is then quantised exactly as jetfp8_quantize_act
+// quantises it, and the optional bf16 output is that same value.
 //
-// Layout of the work: a warp takes a 256-column chunk of one row, lane l the
-// eight values 8l .. 8l+7, loaded and stored as 16-byte vectors.  A 1x128
-// group is then one half-warp: its amax takes four shuffles and its codes
-// leave as one contiguous 128-byte store.
+// Layout of the work: a lane holds eight consecutive values (one 16-byte
+// vector) of a 256-column chunk, so a 1x128 group is one half-warp: its
+// amax takes four shuffles and its codes leave as one contiguous 128-byte
+// store.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <cstdint>
@@ -32,56 +30,20 @@ namespace {
 constexpr int PR_THREADS = 256;
 constexpr int PR_WARPS = PR_THREADS / 32;
 
-// 2^k for -126 <= k <= 127 (unsigned arithmetic: other k, from lanes whose
-// result is discarded, give some bit pattern without overflow)
-__device__ __forceinline__ float pow2_normal(int k)
+// Hardware approximations of 2^x and 1/x (deterministic; the relative
+// error of each is a few fp32 ulps, subnormal results kept).
+__device__ __forceinline__ float ex2_approx(float x)
 {
-    return __uint_as_float((static_cast<uint32_t>(k) + 127u) << 23);
+    float r;
+    asm("ex2.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
 }
 
-// e^x in fp32 for two values at once: Cody-Waite range reduction
-// x = n ln2 + r with n = rint(x / ln2), |r| <= ln2 / 2; e^r from its degree-7
-// Taylor polynomial in Horner form with fused multiply-adds; then the scaling
-// by 2^n in two exact steps.  ln2 is split into a head with 16 significant
-// bits (45426 / 2^16, so n * head is exact) and the rounded remainder.
-// x >= 89 gives +inf, x < -87 gives +0, NaN stays NaN.  Every multiply and
-// fused multiply-add is one packed fp32x2 operation, whose lanes round
-// exactly as the scalar operation would (fma(-n, c, x) is written
-// fma(n, -c, x): the same product, the same rounding); lanes outside the
-// range are replaced at the end.
-__device__ __forceinline__ void exp_f32x2(float x0, float x1, float &e0, float &e1)
+__device__ __forceinline__ float rcp_approx(float x)
 {
-    using namespace ptx;
-    auto dup = [](float c) { return pack_f32x2(c, c); };
-    const uint64_t x = pack_f32x2(x0, x1);
-    const uint64_t t = mul_f32x2(x, dup(1.44269502f));
-    const float n0 = rintf(lo_f32(t)), n1 = rintf(hi_f32(t));
-    const uint64_t n = pack_f32x2(n0, n1);
-    uint64_t r = fma2_f32x2(n, dup(-0.693145751953125f), x);
-    r = fma2_f32x2(n, dup(-1.42860677e-06f), r);
-    uint64_t p = fma2_f32x2(dup(0.000198412701f), r, dup(0.00138888892f));
-    p = fma2_f32x2(p, r, dup(0.00833333377f));
-    p = fma2_f32x2(p, r, dup(0.0416666679f));
-    p = fma2_f32x2(p, r, dup(0.166666672f));
-    p = fma2_f32x2(p, r, dup(0.5f));
-    p = fma2_f32x2(p, r, dup(1.0f));
-    p = fma2_f32x2(p, r, dup(1.0f));
-    const int i0 = __float2int_rz(n0), i1 = __float2int_rz(n1);   // exact in range, saturating outside
-    const int h0 = i0 / 2, h1 = i1 / 2;
-    const uint64_t s1 = pack_f32x2(pow2_normal(h0), pow2_normal(h1));
-    const uint64_t s2 = pack_f32x2(pow2_normal(i0 - h0), pow2_normal(i1 - h1));
-    const uint64_t e = mul_f32x2(mul_f32x2(p, s1), s2);
-    auto fix = [](float xv, float ev) {
-        if (xv != xv)
-            return xv;
-        if (xv >= 89.0f)
-            return __int_as_float(0x7f800000);
-        if (xv < -87.0f)
-            return 0.0f;
-        return ev;
-    };
-    e0 = fix(x0, lo_f32(e));
-    e1 = fix(x1, hi_f32(e));
+    float r;
+    asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
 }
 
 // Round eight fp32 values to bf16 (nearest even), two per conversion: the
@@ -98,13 +60,20 @@ __device__ __forceinline__ void round_bf16x8(const float (&v)[8], uint32_t (&w)[
 }
 
 // ---------------------------------------------------------------------------
-// RMSNorm: one warp per row.  Pass 1 sums the squares: lane l adds, in order,
-// the squares of its chunks' values (chunk 32 j + l, j = 0, 1, ...), then the
-// lanes combine by butterfly (partner distance 16, 8, 4, 2, 1).  Pass 2
-// re-reads the row (from cache), forms y = bf16((x * rstd) * gamma) and
-// quantises it.  Both passes are unrolled four chunks deep so that each warp
-// keeps several loads in flight; the additions stay in chunk order.
+// RMSNorm.  The sum of squares of a row: each thread adds, in order, the
+// squares of its chunks' values (with four warps per row: even and odd
+// values in two chains, added at the end); the lanes of a warp combine by butterfly
+// (partner distance 16, 8, 4, 2, 1); the warps of the row then add up in
+// warp order.  y = bf16((x * rstd) * gamma) is then quantised per 1x128
+// group.  Rows of up to RN_REG_MAX_H columns: four warps per row (two rows
+// per block), each thread's 16-byte chunks t, t + 128, ... held in registers
+// between the two steps, so the row is read from memory once.  Wider rows:
+// one warp per row, the row read a second time (from cache).
 // ---------------------------------------------------------------------------
+constexpr int RN_ROW_THREADS = 128;
+constexpr int RN_ROWS = PR_THREADS / RN_ROW_THREADS;
+constexpr int64_t RN_REG_MAX_H = 16384;      // 16 chunks of 8 values per thread
+
 __device__ __forceinline__ float sum_squares8(float acc, const uint4 &c)
 {
     float f[8];
@@ -117,9 +86,105 @@ __device__ __forceinline__ float sum_squares8(float acc, const uint4 &c)
     return acc;
 }
 
-__global__ void __launch_bounds__(PR_THREADS)
+__device__ __forceinline__ uint64_t sum_squares8x2(uint64_t acc2, const uint4 &c)
+{
+    float f[8];
+    unpack8(c, f);
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+        const uint64_t x2 = ptx::pack_f32x2(f[e], f[e + 1]);
+        ptx::fma_f32x2(acc2, x2, x2);
+    }
+    return acc2;
+}
+
+__device__ __forceinline__ float rms_rstd(float sum_sq, int64_t H, float eps)
+{
+    const float ms = __fdiv_rn(sum_sq, static_cast<float>(H));
+    return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+}
+
+// y = bf16((x * rstd) * gamma) of one 16-byte chunk c (eight values) of a
+// row: stored to y and / or quantised (the chunk's half-warp is its group)
+__device__ __forceinline__ void rms_chunk_out(const uint4 &xc, const uint4 &gc, float rstd, int64_t row, int64_t c,
+                                              int64_t M, int64_t H, uint8_t *__restrict__ q, float *__restrict__ s,
+                                              uint4 *__restrict__ y, int lane)
+{
+    float f[8], g[8], u[8], v[8];
+    unpack8(xc, f);
+    unpack8(gc, g);
+    // (x * rstd) * gamma, two values per packed multiply (each lane rounded
+    // as the scalar multiply)
+    const uint64_t r2 = ptx::pack_f32x2(rstd, rstd);
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+        const uint64_t xr2 = ptx::mul_f32x2(ptx::pack_f32x2(f[e], f[e + 1]), r2);
+        const uint64_t y2 = ptx::mul_f32x2(xr2, ptx::pack_f32x2(g[e], g[e + 1]));
+        u[e] = ptx::lo_f32(y2);
+        u[e + 1] = ptx::hi_f32(y2);
+    }
+    uint32_t w[4];
+    round_bf16x8(u, w, v);
+    if (y)
+        y[row * (H >> 3) + c] = make_uint4(w[0], w[1], w[2], w[3]);
+    if (q)
+        quantize8_halfwarp(v, q + row * H + 8 * c, s + (c >> 4) * M + row, lane);
+}
+
+// (rows of up to 4096 columns: capped for five blocks per SM, +3 % measured)
+template <int JMAX>
+__global__ void __launch_bounds__(PR_THREADS, JMAX <= 4 ? 5 : 1)
 rmsnorm_quantize_kernel(const uint4 *__restrict__ x, const uint4 *__restrict__ gamma, float eps, int64_t M,
                         int64_t H, uint8_t *__restrict__ q, float *__restrict__ s, uint4 *__restrict__ y)
+{
+    __shared__ float part[RN_ROWS][RN_ROW_THREADS / 32];
+    const int lane = threadIdx.x & 31;
+    const int t = threadIdx.x % RN_ROW_THREADS;
+    const int r_in_block = threadIdx.x / RN_ROW_THREADS;
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * RN_ROWS + r_in_block;
+    const bool live = row < M;                    // no early exit: the block meets at a barrier
+    const int64_t H8 = H >> 3;
+    const uint4 *xr = x + (live ? row : 0) * H8;
+
+    // chunks t + 128 j below H8; H8 is a multiple of 32, so a warp's lanes
+    // are all in or all out
+    uint4 v[JMAX];
+#pragma unroll
+    for (int j = 0; j < JMAX; ++j)
+        if (live && t + RN_ROW_THREADS * j < H8)
+            v[j] = __ldg(xr + t + RN_ROW_THREADS * j);
+    // squares summed as two interleaved fp32 chains (even and odd values,
+    // one packed fused multiply-add per pair), then added
+    uint64_t acc2 = 0ull;
+#pragma unroll
+    for (int j = 0; j < JMAX; ++j)
+        if (live && t + RN_ROW_THREADS * j < H8)
+            acc2 = sum_squares8x2(acc2, v[j]);
+    float acc = __fadd_rn(ptx::lo_f32(acc2), ptx::hi_f32(acc2));
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1)
+        acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, d));
+    if (lane == 0)
+        part[r_in_block][t >> 5] = acc;
+    __syncthreads();
+    float sum_sq = part[r_in_block][0];
+#pragma unroll
+    for (int w = 1; w < RN_ROW_THREADS / 32; ++w)
+        sum_sq = __fadd_rn(sum_sq, part[r_in_block][w]);
+    if (!live)
+        return;
+    const float rstd = rms_rstd(sum_sq, H, eps);
+#pragma unroll
+    for (int j = 0; j < JMAX; ++j) {
+        const int64_t c = t + RN_ROW_THREADS * j;
+        if (c < H8)
+            rms_chunk_out(v[j], __ldg(gamma + c), rstd, row, c, M, H, q, s, y, lane);
+    }
+}
+
+__global__ void __launch_bounds__(PR_THREADS)
+rmsnorm_quantize_wide_kernel(const uint4 *__restrict__ x, const uint4 *__restrict__ gamma, float eps, int64_t M,
+                             int64_t H, uint8_t *__restrict__ q, float *__restrict__ s, uint4 *__restrict__ y)
 {
     const int lane = threadIdx.x & 31;
     const int64_t row = static_cast<int64_t>(blockIdx.x) * PR_WARPS + (threadIdx.x >> 5);
@@ -128,7 +193,6 @@ rmsnorm_quantize_kernel(const uint4 *__restrict__ x, const uint4 *__restrict__ g
     const int64_t H8 = H >> 3;
     const uint4 *xr = x + row * H8;
     const int nj = static_cast<int>(H >> 8);
-
     float acc = 0.0f;
 #pragma unroll 4
     for (int j = 0; j < nj; ++j)
@@ -136,31 +200,11 @@ rmsnorm_quantize_kernel(const uint4 *__restrict__ x, const uint4 *__restrict__ g
 #pragma unroll
     for (int d = 16; d >= 1; d >>= 1)
         acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, d));
-    const float ms = __fdiv_rn(acc, static_cast<float>(H));
-    const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
-
+    const float rstd = rms_rstd(acc, H, eps);
 #pragma unroll 4
     for (int j = 0; j < nj; ++j) {
         const int64_t c = 32 * j + lane;
-        float f[8], g[8], u[8], v[8];
-        unpack8(__ldg(xr + c), f);
-        unpack8(__ldg(gamma + c), g);
-        // (x * rstd) * gamma, two values per packed multiply (each lane
-        // rounded as the scalar multiply)
-        const uint64_t r2 = ptx::pack_f32x2(rstd, rstd);
-#pragma unroll
-        for (int e = 0; e < 8; e += 2) {
-            const uint64_t xr2 = ptx::mul_f32x2(ptx::pack_f32x2(f[e], f[e + 1]), r2);
-            const uint64_t y2 = ptx::mul_f32x2(xr2, ptx::pack_f32x2(g[e], g[e + 1]));
-            u[e] = ptx::lo_f32(y2);
-            u[e + 1] = ptx::hi_f32(y2);
-        }
-        uint32_t w[4];
-        round_bf16x8(u, w, v);
-        if (y)
-            y[row * H8 + c] = make_uint4(w[0], w[1], w[2], w[3]);
-        if (q)
-            quantize8_halfwarp(v, q + row * H + 8 * c, s + (c >> 4) * M + row, lane);
+        rms_chunk_out(__ldg(xr + c), __ldg(gamma + c), rstd, row, c, M, H, q, s, y, lane);
     }
 }
 
@@ -168,7 +212,18 @@ rmsnorm_quantize_kernel(const uint4 *__restrict__ x, const uint4 *__restrict__ g
 // SwiGLU of a gate_up output [M][2I] (gate = columns 0..I-1, up = I..2I-1):
 // y = bf16( (g * (1 / (1 + e^-g))) * u ).  A warp handles one 256-column
 // chunk of one row per iteration (grid-stride over all chunks).
+//
+// Accuracy: -g log2 e is rounded once, which moves the exponent by at most
+// 2^-24 |g log2 e| <= 2^-17 where 2^(-g log2 e) is finite and normal, i.e. a
+// relative error below 2^-17.5 in e^-g; the hardware 2^x and 1/x add a few
+// fp32 ulps each and the three roundings (1 + e^-g, g * sigmoid, * u) one
+// ulp each.  The fp32 result is within 2^-16 of silu(g) u relative, well
+// inside half a bf16 ulp (2^-9), so its bf16 rounding is within one bf16 ulp
+// of the exact value.  Below g = -87 the reciprocal's result leaves fp32's
+// normal range and ends at 0 (e^-g overflowing); there the exact value is
+// below 2^-119 |u|.
 // ---------------------------------------------------------------------------
+constexpr float LOG2E = 1.44269502f;              // log2(e) rounded to fp32
 __global__ void __launch_bounds__(PR_THREADS)
 swiglu_quantize_kernel(const uint4 *__restrict__ gu, int64_t M, int64_t I, uint8_t *__restrict__ q,
                        float *__restrict__ s, uint4 *__restrict__ y)
@@ -187,10 +242,10 @@ swiglu_quantize_kernel(const uint4 *__restrict__ gu, int64_t M, int64_t I, uint8
         unpack8(__ldg(gu + row * in_row + out_row + c), u);
 #pragma unroll
         for (int e = 0; e < 8; e += 2) {
-            // 1 / (1 + e^-g): the correctly rounded reciprocal is the IEEE quotient
-            float x0, x1;
-            exp_f32x2(-g[e], -g[e + 1], x0, x1);
-            const float s0 = __frcp_rn(__fadd_rn(1.0f, x0)), s1 = __frcp_rn(__fadd_rn(1.0f, x1));
+            // sigmoid(g) = 1 / (1 + 2^(-g log2 e))
+            const uint64_t a = ptx::mul_f32x2(ptx::pack_f32x2(g[e], g[e + 1]), ptx::pack_f32x2(-LOG2E, -LOG2E));
+            const float s0 = rcp_approx(__fadd_rn(1.0f, ex2_approx(ptx::lo_f32(a))));
+            const float s1 = rcp_approx(__fadd_rn(1.0f, ex2_approx(ptx::hi_f32(a))));
             const uint64_t gs = ptx::mul_f32x2(ptx::pack_f32x2(g[e], g[e + 1]), ptx::pack_f32x2(s0, s1));
             const uint64_t tu = ptx::mul_f32x2(gs, ptx::pack_f32x2(u[e], u[e + 1]));
             t[e] = ptx::lo_f32(tu);
@@ -210,9 +265,25 @@ swiglu_quantize_kernel(const uint4 *__restrict__ gu, int64_t M, int64_t I, uint8
 cudaError_t launch_rmsnorm_quantize(const void *x, const void *gamma, float eps, int64_t M, int64_t H, uint8_t *q,
                                     float *s, void *y, cudaStream_t stream)
 {
-    const int64_t blocks = (M + PR_WARPS - 1) / PR_WARPS;
-    rmsnorm_quantize_kernel<<<static_cast<unsigned>(blocks), PR_THREADS, 0, stream>>>(
-        static_cast<const uint4 *>(x), static_cast<const uint4 *>(gamma), eps, M, H, q, s, static_cast<uint4 *>(y));
+    const uint4 *xv = static_cast<const uint4 *>(x);
+    const uint4 *gv = static_cast<const uint4 *>(gamma);
+    uint4 *yv = static_cast<uint4 *>(y);
+    if (H > RN_REG_MAX_H) {
+        const int64_t blocks = (M + PR_WARPS - 1) / PR_WARPS;
+        rmsnorm_quantize_wide_kernel<<<static_cast<unsigned>(blocks), PR_THREADS, 0, stream>>>(xv, gv, eps, M, H, q,
+                                                                                               s, yv);
+        return cudaGetLastError();
+    }
+    const unsigned blocks = static_cast<unsigned>((M + RN_ROWS - 1) / RN_ROWS);
+    // chunks of 8 values per thread: H / 8 / 128, rounded up
+    if (H <= 4096)
+        rmsnorm_quantize_kernel<4><<<blocks, PR_THREADS, 0, stream>>>(xv, gv, eps, M, H, q, s, yv);
+    else if (H <= 5120)
+        rmsnorm_quantize_kernel<5><<<blocks, PR_THREADS, 0, stream>>>(xv, gv, eps, M, H, q, s, yv);
+    else if (H <= 8192)
+        rmsnorm_quantize_kernel<8><<<blocks, PR_THREADS, 0, stream>>>(xv, gv, eps, M, H, q, s, yv);
+    else
+        rmsnorm_quantize_kernel<16><<<blocks, PR_THREADS, 0, stream>>>(xv, gv, eps, M, H, q, s, yv);
     return cudaGetLastError();
 }
 

@@ -141,7 +141,8 @@ JETFP8_API jetfp8_status jetfp8_rmsnorm_quantize_act(const void *x, const void *
  * gu holds gate in columns 0..I-1 and up in columns I..2I-1 of each row;
  *   y = silu(g) * u = g / (1 + e^-g) * u,
  * returned as bf16 within one bf16 ulp of the exact value (fp32 in a fixed
- * order, with this library's own fp32 e^x); for g < -87, where the fp32
+ * order, e^-g and the reciprocal from the hardware's fp32 approximations,
+ * whose error stays far inside that bound); for g < -87, where the fp32
  * sigmoid underflows, within 2^-119 |u| of it.  The codes and scales are
  * exactly those jetfp8_quantize_act gives for the returned bf16 y.
  *   gu   : bf16 [M][2I]                    (input)

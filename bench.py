@@ -72,20 +72,20 @@ FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1
 # SHA-256 is recorded here (the kernel and its inline-PTX helpers) and is
 # reported as null once they differ.
 GEMM_TRAFFIC = {"per_launch_bytes": {
-                                     "dgrad:down": 660466944,
-                                     "dgrad:gate_up": 2362561280,
-                                     "dgrad:o": 173986048,
-                                     "dgrad:qkv": 223461376,
-                                     "fprop:down": 719102720,
-                                     "fprop:gate_up": 1396372992,
-                                     "fprop:o": 175453184,
-                                     "fprop:qkv": 255982080,
-                                     "wgrad:down": 944110848,
-                                     "wgrad:gate_up": 2373840896,
-                                     "wgrad:o": 313657856,
-                                     "wgrad:qkv": 490490368},
+                                     "dgrad:down": 640437504,
+                                     "dgrad:gate_up": 2347882752,
+                                     "dgrad:o": 173171968,
+                                     "dgrad:qkv": 222554112,
+                                     "fprop:down": 679173120,
+                                     "fprop:gate_up": 1346667776,
+                                     "fprop:o": 174824704,
+                                     "fprop:qkv": 253932032,
+                                     "wgrad:down": 925304064,
+                                     "wgrad:gate_up": 2332539648,
+                                     "wgrad:o": 305678848,
+                                     "wgrad:qkv": 482245632},
                 "sources": ("gemm.cu", "ptx.cuh"),
-                "sha256": "fe5aafad1f6dfedc66dcad05eddd5a1d711cd96923818022542b3c6ccc4cfe55"}
+                "sha256": "c9fdf7c2b8db675b26c4a356681714bf6557ce8d66718743c037b8f1203cf71e"}
 
 
 def gemm_sources_sha256() -> str:

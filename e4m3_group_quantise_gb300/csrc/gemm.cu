@@ -397,12 +397,23 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                     }
                     float *dst = scl + ss * L::SCALE_FLOATS;
                     const float *sa_g = args.sa + static_cast<int64_t>(g) * args.rows;
-#pragma unroll
-                    for (int i = 0; i < BM / 32; ++i) {
-                        const int r = i * 32 + lane;
-                        const int row = tm * BM + r;
+                    // lane l: rows 4l .. 4l+3 of the tile, one 16-byte copy when
+                    // the row count keeps them 16-byte aligned (every row count
+                    // that is a multiple of 4), else four 4-byte copies (one
+                    // 16-byte copy instead of four measured +2 % on Fprop / Dgrad:
+                    // fewer copies queue in front of the promotion warps' shared
+                    // memory traffic)
+                    const int r = 4 * lane;
+                    const int row = tm * BM + r;
+                    if ((args.rows & 3) == 0) {
                         const bool in = row < args.rows;
-                        ptx::cp_async_4(dst + r, in ? sa_g + row : args.sa, in ? 4u : 0u);
+                        ptx::cp_async_16z(dst + r, in ? sa_g + row : args.sa, in ? 16u : 0u);
+                    } else {
+#pragma unroll 1
+                        for (int e = 0; e < 4; ++e) {
+                            const bool in = row + e < args.rows;
+                            ptx::cp_async_4(dst + r + e, in ? sa_g + row + e : args.sa, in ? 4u : 0u);
+                        }
                     }
                     // the block scales of the tile's 128-column blocks (per-column
                     // scales never come here: the TMA producer copies those)

@@ -237,10 +237,20 @@ class Step:
             d["dw"] = e(n, k, dt=torch.bfloat16)
             self.p[name] = d
 
-    def launches(self, d):
+    def quant_weights(self):
+        """Every projection's master weight quantised (codes + transposed
+        codes) in one grouped launch."""
+        ds = list(self.p.values())
+        self.jf.jetfp8_quantize_weight_group([d["w"] for d in ds], [d["qw"] for d in ds], [d["sw"] for d in ds],
+                                             [d["qwt"] for d in ds])
+
+    def launches(self, d, weight=False):
+        """One projection's launches; with `weight`, its own weight
+        quantisation first (the end-to-end path, whose weights arrive from
+        the host one projection at a time)."""
         jf = self.jf
-        return (
-            ("quant_w", lambda: jf.jetfp8_quantize_weight(d["w"], d["qw"], d["sw"], d["qwt"])),
+        own_w = (("quant_w", lambda: jf.jetfp8_quantize_weight(d["w"], d["qw"], d["sw"], d["qwt"])),) if weight else ()
+        return own_w + (
             ("quant_x_dual", lambda: jf.jetfp8_quantize_act_dual(d["x"], d["qx"], d["sx"], d["qxt"], d["sxt"])),
             ("quant_dy_dual", lambda: jf.jetfp8_quantize_act_dual(d["dy"], d["qdy"], d["sdy"], d["qdyt"],
                                                                   d["sdyt"])),
@@ -260,13 +270,32 @@ class Step:
         quantisations run there in projection order, ahead of the GEMMs that
         need them, so they can also fill GEMM tails.  The current stream waits
         for the others at the end.  With `events`, every launch is bracketed
-        by (start, end) events on the stream it runs on."""
+        by (start, end) events on the stream it runs on.  The step starts
+        with one grouped launch that quantises every projection's weight (all
+        master weights are resident, so one launch shares its start-up and
+        last stores among them)."""
         main = torch.cuda.current_stream()
         for st in (side, quant):
             if st is not None:
                 st.wait_stream(main)
+        ws = quant if quant is not None else main
+        with torch.cuda.stream(ws):
+            ev0 = ev1 = None
+            if events is not None:
+                ev0 = torch.cuda.Event(enable_timing=True)
+                ev0.record(ws)
+            self.quant_weights()
+            if events is not None:
+                ev1 = torch.cuda.Event(enable_timing=True)
+                ev1.record(ws)
+                events.append(("all", "quant_w", ev0, ev1))
+        all_w_ready = None
+        if ws is not main:
+            all_w_ready = torch.cuda.Event()
+            all_w_ready.record(ws)
         for name, d in self.p.items():
-            x_ready = dy_ready = w_ready = None
+            x_ready = dy_ready = None
+            w_ready = all_w_ready
             for kind, fn in self.launches(d):
                 if quant is not None and kind.startswith("quant"):
                     s = quant
@@ -390,6 +419,8 @@ def time_e2e(step, steps, device):
     # Per projection: copy its inputs in on a copy stream, compute on the
     # current stream once they have landed, copy its results out on a third
     # stream; the next projection's inputs travel while this one computes.
+    # The weights arrive one projection at a time, so each is quantised on its
+    # own as it lands (no grouped launch here).
     # Reuse across steps is ordered by events (inputs are overwritten only
     # after the previous step's kernels read them, results only after the
     # previous step's copies took them).
@@ -412,7 +443,7 @@ def time_e2e(step, steps, device):
             main.wait_event(landed)
             if copied_out[name] is not None:
                 main.wait_event(copied_out[name])
-            for _, fn in step.launches(d):
+            for _, fn in step.launches(d, weight=True):
                 fn()
             computed = torch.cuda.Event()
             computed.record(main)

@@ -17,6 +17,7 @@ from .jetfp8 import (  # noqa: F401
     jetfp8_quantize_act_dual,
     jetfp8_quantize_act_transposed,
     jetfp8_quantize_weight,
+    jetfp8_quantize_weight_group,
     jetfp8_rmsnorm_quantize_act,
     jetfp8_swiglu_quantize_act,
     jetfp8_status_string,
@@ -26,6 +27,7 @@ from .jetfp8 import (  # noqa: F401
     quantize_act_dual,
     quantize_act_transposed,
     quantize_weight,
+    quantize_weights,
     rmsnorm_quantize_act,
     swiglu_quantize_act,
 )

@@ -257,8 +257,9 @@ JETFP8_API jetfp8_status jetfp8_e4m3_encode_range(uint32_t first, int64_t count,
         jetfp8::launch_e4m3_encode_range(first, count, codes, dev->sm_count, static_cast<cudaStream_t>(stream)));
 }
 
-JETFP8_API jetfp8_status jetfp8_quantize_weight(const void *w, int64_t N, int64_t K, uint8_t *q, float *s,
-                                                uint8_t *qt, void *stream)
+namespace {
+// One weight tensor's host-side checks (shared by the single and grouped calls).
+jetfp8_status check_weight(const void *w, int64_t N, int64_t K, uint8_t *q, float *s, uint8_t *qt)
 {
     if (N <= 0 || K <= 0 || N % 128 != 0 || K % 128 != 0 || !dims_ok(N, K) || K / 128 > 65535 ||
         N / 128 > 65535)
@@ -272,6 +273,16 @@ JETFP8_API jetfp8_status jetfp8_quantize_weight(const void *w, int64_t N, int64_
     const Range ins[1] = {range_of(w, N * K * 2)};
     if (any_overlap(outs, qt ? 3 : 2, ins, 1))
         return JETFP8_ERR_INVALID_VALUE;
+    return JETFP8_OK;
+}
+}  // namespace
+
+JETFP8_API jetfp8_status jetfp8_quantize_weight(const void *w, int64_t N, int64_t K, uint8_t *q, float *s,
+                                                uint8_t *qt, void *stream)
+{
+    const jetfp8_status chk = check_weight(w, N, K, q, s, qt);
+    if (chk != JETFP8_OK)
+        return chk;
     const DeviceInfo *dev = nullptr;
     jetfp8_status st = current_device(&dev);
     if (st != JETFP8_OK)
@@ -281,6 +292,46 @@ JETFP8_API jetfp8_status jetfp8_quantize_weight(const void *w, int64_t N, int64_
         return JETFP8_ERR_UNSUPPORTED_DEVICE;
     return launch_status(jetfp8::launch_quantize_weight(w, N, K, q, s, qt, g_encode, dev->err_word, dev->sm_count,
                                                         static_cast<cudaStream_t>(stream)));
+}
+
+JETFP8_API jetfp8_status jetfp8_quantize_weight_group(int count, const void *const *w, const int64_t *N,
+                                                      const int64_t *K, uint8_t *const *q, float *const *s,
+                                                      uint8_t *const *qt, void *stream)
+{
+    if (count < 0 || count > JETFP8_WEIGHT_GROUP_MAX)
+        return JETFP8_ERR_SHAPE;
+    if (count == 0)
+        return JETFP8_OK;
+    if (!w || !N || !K || !q || !s || !qt)
+        return JETFP8_ERR_INVALID_VALUE;
+    for (int t = 0; t < count; ++t) {
+        const jetfp8_status chk = check_weight(w[t], N[t], K[t], q[t], s[t], qt[t]);
+        if (chk != JETFP8_OK)
+            return chk;
+    }
+    // no output of one entry may overlap an input or output of another
+    for (int t = 0; t < count; ++t) {
+        const Range outs[3] = {range_of(q[t], N[t] * K[t]), range_of(s[t], (N[t] / 128) * (K[t] / 128) * 4),
+                               range_of(qt[t], qt[t] ? N[t] * K[t] : 0)};
+        for (int u = 0; u < count; ++u) {
+            if (u == t)
+                continue;
+            const Range others[4] = {range_of(w[u], N[u] * K[u] * 2), range_of(q[u], N[u] * K[u]),
+                                     range_of(s[u], (N[u] / 128) * (K[u] / 128) * 4),
+                                     range_of(qt[u], qt[u] ? N[u] * K[u] : 0)};
+            if (any_overlap(outs, qt[t] ? 3 : 2, others, qt[u] ? 4 : 3))
+                return JETFP8_ERR_INVALID_VALUE;
+        }
+    }
+    const DeviceInfo *dev = nullptr;
+    jetfp8_status st = current_device(&dev);
+    if (st != JETFP8_OK)
+        return st;
+    std::call_once(g_encode_once, init_encode);
+    if (g_encode == nullptr)
+        return JETFP8_ERR_UNSUPPORTED_DEVICE;
+    return launch_status(jetfp8::launch_quantize_weight_group(count, w, N, K, q, s, qt, g_encode, dev->err_word,
+                                                              dev->sm_count, static_cast<cudaStream_t>(stream)));
 }
 
 JETFP8_API jetfp8_status jetfp8_rmsnorm_quantize_act(const void *x, const void *gamma, float eps, int64_t M,

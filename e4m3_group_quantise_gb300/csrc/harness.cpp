@@ -215,11 +215,36 @@ struct Streams {
     }
 };
 
-// One step.  With a side stream, each projection's dY quantisation and Wgrad
-// run there (Wgrad after X's transposed codes exist; Dgrad on the main stream
-// after dY's codes exist), so one GEMM's last partial wave is filled by the
-// other's tiles.  With `timing`, every launch is bracketed by timing events
-// recorded into timing[kind] (serial pass: main stream only).
+// Every projection's weight (codes + transposed codes) in one grouped launch.
+jetfp8_status quantize_all_weights(std::vector<Proj> &projs, cudaStream_t s)
+{
+    const void *w[JETFP8_WEIGHT_GROUP_MAX];
+    int64_t n[JETFP8_WEIGHT_GROUP_MAX], k[JETFP8_WEIGHT_GROUP_MAX];
+    uint8_t *q[JETFP8_WEIGHT_GROUP_MAX], *qt[JETFP8_WEIGHT_GROUP_MAX];
+    float *sc[JETFP8_WEIGHT_GROUP_MAX];
+    const int count = static_cast<int>(projs.size());
+    if (count > JETFP8_WEIGHT_GROUP_MAX)
+        return JETFP8_ERR_SHAPE;
+    for (int i = 0; i < count; ++i) {
+        w[i] = projs[i].w;
+        n[i] = projs[i].n;
+        k[i] = projs[i].k;
+        q[i] = projs[i].qw;
+        sc[i] = projs[i].sw;
+        qt[i] = projs[i].qwt;
+    }
+    return jetfp8_quantize_weight_group(count, w, n, k, q, sc, qt, s);
+}
+
+// One step on device-resident inputs.  It starts with one grouped launch that
+// quantises every projection's weight (the master weights are all resident,
+// so they share one launch's start-up and last stores); then per projection
+// the X and dY quantisations and the three GEMMs.  With a side stream, each
+// projection's dY quantisation and Wgrad run there (Wgrad after X's
+// transposed codes exist; Dgrad on the main stream after dY's codes exist),
+// so one GEMM's last partial wave is filled by the other's tiles.  With
+// `timing`, every launch is bracketed by timing events recorded into
+// timing[kind] (serial pass: main stream only).
 void step(std::vector<Proj> &projs, Streams &st, bool two_streams,
           std::vector<std::pair<Kind, std::pair<cudaEvent_t, cudaEvent_t>>> *timing)
 {
@@ -229,9 +254,22 @@ void step(std::vector<Proj> &projs, Streams &st, bool two_streams,
         cuda_ok(cudaEventRecord(e, st.main), "record");
         cuda_ok(cudaStreamWaitEvent(st.side, e, 0), "wait");
     }
+    {
+        cudaEvent_t t0 = nullptr, t1 = nullptr;
+        if (timing) {
+            cuda_ok(cudaEventCreate(&t0), "cudaEventCreate");
+            cuda_ok(cudaEventCreate(&t1), "cudaEventCreate");
+            cuda_ok(cudaEventRecord(t0, st.main), "record");
+        }
+        lib_ok(quantize_all_weights(projs, st.main), "quant_w (grouped)");
+        if (timing) {
+            cuda_ok(cudaEventRecord(t1, st.main), "record");
+            timing->push_back({QUANT_W, {t0, t1}});
+        }
+    }
     for (Proj &p : projs) {
         cudaEvent_t x_ready = nullptr, dy_ready = nullptr;
-        for (int k = 0; k < NKIND; ++k) {
+        for (int k = QUANT_X_DUAL; k < NKIND; ++k) {
             const Kind kind = static_cast<Kind>(k);
             cudaStream_t s = (two_streams && (kind == QUANT_DY_DUAL || kind == WGRAD)) ? st.side : st.main;
             if (two_streams && kind == DGRAD)
@@ -401,7 +439,9 @@ int main(int argc, char **argv)
         cudaEventDestroy(t.second.first);
         cudaEventDestroy(t.second.second);
     }
-    int launches = (warmup + steps + serial) * 4 * NKIND;
+    // device-resident steps: one grouped weight launch + five per projection;
+    // end-to-end steps (below): six per projection
+    int launches = (warmup + steps + serial) * (1 + static_cast<int>(projs.size()) * (NKIND - 1));
 
     // ---- end to end from pinned host memory
     double e2e_ms = 0.0;
@@ -420,6 +460,8 @@ int main(int argc, char **argv)
         // Per projection: inputs in on s_in (after the previous step's kernels
         // have read them), compute on the main stream once they have landed
         // (and the previous step's results have left), results out on s_out.
+        // The weights arrive one projection at a time, so each is quantised
+        // on its own as it lands (no grouped launch here).
         auto one = [&]() {
             for (size_t i = 0; i < np; ++i) {
                 Proj &p = projs[i];
@@ -457,7 +499,7 @@ int main(int argc, char **argv)
         float ms = 0.0f;
         cuda_ok(cudaEventElapsedTime(&ms, a, b), "elapsed");
         e2e_ms = ms / e2e_steps;
-        launches += (1 + e2e_steps) * 4 * NKIND;
+        launches += (1 + e2e_steps) * static_cast<int>(projs.size()) * NKIND;
     }
 
     // ---- one JSON line

@@ -31,6 +31,11 @@ cudaError_t launch_quantize_act_dual(const void *x, int64_t M, int64_t K, uint8_
 cudaError_t launch_quantize_weight(const void *w, int64_t N, int64_t K, uint8_t *q, float *s, uint8_t *qt,
                                    PFN_cuTensorMapEncodeTiled_v12000 encode, uint32_t *err, int sm_count,
                                    cudaStream_t stream);
+// 1 <= count <= 8 weight tensors in one launch (arrays of count host entries)
+cudaError_t launch_quantize_weight_group(int count, const void *const *w, const int64_t *N, const int64_t *K,
+                                         uint8_t *const *q, float *const *s, uint8_t *const *qt,
+                                         PFN_cuTensorMapEncodeTiled_v12000 encode, uint32_t *err, int sm_count,
+                                         cudaStream_t stream);
 cudaError_t launch_e4m3_encode_range(uint32_t first, int64_t count, uint8_t *codes, int sm_count,
                                      cudaStream_t stream);
 

@@ -224,8 +224,10 @@ quantize_act_t_kernel(const uint4 *__restrict__ x, int64_t M, int64_t C, uint8_t
 }
 
 // ---------------------------------------------------------------------------
-// 128x128 weight blocks.  Persistent CTAs (two per SM) walk the blocks in
-// row-major order, block b, b + gridDim.x, ...; each block arrives by two
+// 128x128 weight blocks of one or several weight tensors (a group: every
+// master weight of a step in one launch).  The tensors' blocks are numbered
+// one after the other, each tensor's in row-major order.  Persistent CTAs (two
+// per SM) walk them, block b, b + gridDim.x, ...; each block arrives by two
 // bulk tensor copies (TMA, 128-byte swizzle, as in the dual quantiser) into
 // one of two shared-memory stages, so the next block is in flight while this
 // one is encoded.  Per block (8 warps):
@@ -249,6 +251,7 @@ quantize_act_t_kernel(const uint4 *__restrict__ x, int64_t M, int64_t C, uint8_t
 constexpr int QW_THREADS = 256;
 constexpr int QW_STAGES = 2;
 constexpr int QW_CODE_PITCH = 160;           // bytes per code-tile row: row-pass writes in two wavefronts
+constexpr int QW_GROUP_MAX = 8;              // weight tensors per launch (JETFP8_WEIGHT_GROUP_MAX)
 
 struct WeightSmem {
     uint8_t tile[QW_STAGES][2][128][128];    // per stage: two 64-column halves, 128-byte swizzle
@@ -263,32 +266,57 @@ __device__ __forceinline__ const uint8_t *weight_chunk(const WeightSmem &sm, int
     return &sm.tile[stage][c >> 3][r][((c & 7) ^ (r & 7)) << 4];
 }
 
+// The tensors of one launch: tensor t's blocks are first_block[t] ..
+// first_block[t + 1] - 1 of the launch's numbering.
+struct WeightGroup {
+    CUtensorMap map[QW_GROUP_MAX];           // W_t [N_t][K_t] bf16 as 128-row x 64-column boxes, 128-byte swizzle
+    int64_t N[QW_GROUP_MAX], K[QW_GROUP_MAX];
+    uint8_t *q[QW_GROUP_MAX];
+    float *s[QW_GROUP_MAX];
+    uint8_t *qt[QW_GROUP_MAX];               // may be null per tensor
+    int64_t first_block[QW_GROUP_MAX + 1];
+    int count;
+};
 
+// Block blk of the launch: its tensor, and its block row and column there.
+struct WeightBlock {
+    int t;
+    int64_t bn, bk;
+};
+
+__device__ __forceinline__ WeightBlock locate_block(const WeightGroup &grp, int64_t blk)
+{
+    int t = 0;
+    while (t + 1 < grp.count && blk >= grp.first_block[t + 1])
+        ++t;
+    const int64_t local = blk - grp.first_block[t], bk_count = grp.K[t] >> 7;
+    return WeightBlock{t, local / bk_count, local % bk_count};
+}
 
 __global__ void __launch_bounds__(QW_THREADS, 2)
-quantize_weight_kernel(const __grid_constant__ CUtensorMap tmap_w, int64_t N, int64_t K, uint8_t *__restrict__ q,
-                       float *__restrict__ s, uint8_t *__restrict__ qt, uint32_t *__restrict__ err)
+quantize_weight_kernel(const __grid_constant__ WeightGroup grp, uint32_t *__restrict__ err)
 {
     extern __shared__ uint8_t weight_smem_raw[];
     WeightSmem &sm = *reinterpret_cast<WeightSmem *>((reinterpret_cast<uintptr_t>(weight_smem_raw) + 1023) &
                                                      ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t bk_count = K >> 7;
-    const int64_t blocks = (N >> 7) * bk_count;
+    const int64_t blocks = grp.first_block[grp.count];
     const int64_t first = blockIdx.x, stride = gridDim.x;
     constexpr uint32_t TILE_BYTES = 128 * 128 * 2;
 
     auto request = [&](int64_t blk, int stage) {   // one thread: bring block blk into stage
-        const int32_t n0 = static_cast<int32_t>((blk / bk_count) << 7), k0 = static_cast<int32_t>((blk % bk_count) << 7);
+        const WeightBlock b = locate_block(grp, blk);
+        const int32_t n0 = static_cast<int32_t>(b.bn << 7), k0 = static_cast<int32_t>(b.bk << 7);
         ptx::mbar_arrive_expect_tx(&sm.full[stage], TILE_BYTES);
-        ptx::tma_load_2d(&sm.tile[stage][0][0][0], &tmap_w, &sm.full[stage], k0, n0);
-        ptx::tma_load_2d(&sm.tile[stage][1][0][0], &tmap_w, &sm.full[stage], k0 + 64, n0);
+        ptx::tma_load_2d(&sm.tile[stage][0][0][0], &grp.map[b.t], &sm.full[stage], k0, n0);
+        ptx::tma_load_2d(&sm.tile[stage][1][0][0], &grp.map[b.t], &sm.full[stage], k0 + 64, n0);
     };
     if (threadIdx.x == 0) {
         for (int st = 0; st < QW_STAGES; ++st)
             ptx::mbar_init(&sm.full[st], 1);
         ptx::fence_mbar_init();
-        ptx::tma_prefetch_desc(&tmap_w);
+        for (int t = 0; t < grp.count; ++t)
+            ptx::tma_prefetch_desc(&grp.map[t]);
         for (int st = 0; st < QW_STAGES; ++st)
             if (first + st * stride < blocks)
                 request(first + st * stride, st);
@@ -312,7 +340,11 @@ quantize_weight_kernel(const __grid_constant__ CUtensorMap tmap_w, int64_t N, in
                 }
             return;
         }
-        const int64_t n_base = (blk / bk_count) << 7, k_base = (blk % bk_count) << 7;
+        const WeightBlock wb = locate_block(grp, blk);
+        const int64_t N = grp.N[wb.t], K = grp.K[wb.t], bk_count = K >> 7;
+        uint8_t *__restrict__ q = grp.q[wb.t];
+        uint8_t *__restrict__ qt = grp.qt[wb.t];
+        const int64_t n_base = wb.bn << 7, k_base = wb.bk << 7;
 
         // ---- read this lane's 64 values and their amax
         uint4 v[2][4];
@@ -342,7 +374,7 @@ quantize_weight_kernel(const __grid_constant__ CUtensorMap tmap_w, int64_t N, in
             amax = fmaxf(amax, sm.red[i]);
         const GroupScale gs = group_scale(amax);
         if (threadIdx.x == 0)
-            s[(n_base >> 7) * bk_count + (k_base >> 7)] = gs.s;
+            grp.s[wb.t][wb.bn * bk_count + wb.bk] = gs.s;
 
         // ---- encode: codes to q and to the shared code tile
 #pragma unroll
@@ -690,29 +722,49 @@ cudaError_t launch_e4m3_encode_range(uint32_t first, int64_t count, uint8_t *cod
 }  // namespace jetfp8
 
 namespace jetfp8 {
-cudaError_t launch_quantize_weight(const void *w, int64_t N, int64_t K, uint8_t *q, float *s, uint8_t *qt,
-                                   PFN_cuTensorMapEncodeTiled_v12000 encode, uint32_t *err, int sm_count,
-                                   cudaStream_t stream)
+cudaError_t launch_quantize_weight_group(int count, const void *const *w, const int64_t *N, const int64_t *K,
+                                         uint8_t *const *q, float *const *s, uint8_t *const *qt,
+                                         PFN_cuTensorMapEncodeTiled_v12000 encode, uint32_t *err, int sm_count,
+                                         cudaStream_t stream)
 {
-    // W [N][K] bf16 seen as 128-row x 64-column boxes with the 128-byte swizzle
-    CUtensorMap tmap;
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-    cuuint32_t box[2] = {64, 128};
-    cuuint32_t estr[2] = {1, 1};
-    if (encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(w), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    if (count < 1 || count > QW_GROUP_MAX)
         return cudaErrorInvalidValue;
+    WeightGroup grp = {};
+    grp.count = count;
+    grp.first_block[0] = 0;
+    for (int t = 0; t < count; ++t) {
+        // W_t [N][K] bf16 seen as 128-row x 64-column boxes with the 128-byte swizzle
+        cuuint64_t dims[2] = {static_cast<cuuint64_t>(K[t]), static_cast<cuuint64_t>(N[t])};
+        cuuint64_t strides[1] = {static_cast<cuuint64_t>(K[t]) * 2};
+        cuuint32_t box[2] = {64, 128};
+        cuuint32_t estr[2] = {1, 1};
+        if (encode(&grp.map[t], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(w[t]), dims, strides, box,
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+        grp.N[t] = N[t];
+        grp.K[t] = K[t];
+        grp.q[t] = q[t];
+        grp.s[t] = s[t];
+        grp.qt[t] = qt[t];
+        grp.first_block[t + 1] = grp.first_block[t] + (N[t] / 128) * (K[t] / 128);
+    }
     cudaError_t e = cudaFuncSetAttribute(quantize_weight_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(QW_SMEM_BYTES));
     if (e != cudaSuccess)
         return e;
-    const int64_t blocks = (N / 128) * (K / 128);
+    const int64_t blocks = grp.first_block[count];
     const int64_t cap = static_cast<int64_t>(sm_count) * 2;   // two resident CTAs per SM
     const unsigned grid = static_cast<unsigned>(blocks < cap ? blocks : cap);
-    quantize_weight_kernel<<<grid, QW_THREADS, QW_SMEM_BYTES, stream>>>(tmap, N, K, q, s, qt, err);
+    quantize_weight_kernel<<<grid, QW_THREADS, QW_SMEM_BYTES, stream>>>(grp, err);
     return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_weight(const void *w, int64_t N, int64_t K, uint8_t *q, float *s, uint8_t *qt,
+                                   PFN_cuTensorMapEncodeTiled_v12000 encode, uint32_t *err, int sm_count,
+                                   cudaStream_t stream)
+{
+    return launch_quantize_weight_group(1, &w, &N, &K, &q, &s, &qt, encode, err, sm_count, stream);
 }
 
 cudaError_t launch_quantize_act_dual(const void *x, int64_t M, int64_t K, uint8_t *q, float *s, uint8_t *qt,

@@ -59,13 +59,14 @@ def load_library():
     lib.jetfp8_quantize_act.argtypes = [P, I, I, P, P, P]
     lib.jetfp8_quantize_act_transposed.argtypes = [P, I, I, P, P, P]
     lib.jetfp8_quantize_weight.argtypes = [P, I, I, P, P, P, P]
+    lib.jetfp8_quantize_weight_group.argtypes = [S, P, P, P, P, P, P, P]
     lib.jetfp8_quantize_act_dual.argtypes = [P, I, I, P, P, P, P, P]
     lib.jetfp8_rmsnorm_quantize_act.argtypes = [P, P, ctypes.c_float, I, I, P, P, P, P]
     lib.jetfp8_swiglu_quantize_act.argtypes = [P, I, I, P, P, P, P]
     for name in ("jetfp8_gemm_fprop", "jetfp8_gemm_dgrad", "jetfp8_gemm_wgrad"):
         getattr(lib, name).argtypes = [P, P, P, P, P, I, I, I, P]
     for name in ("jetfp8_quantize_act", "jetfp8_quantize_act_transposed", "jetfp8_quantize_weight",
-                 "jetfp8_quantize_act_dual", "jetfp8_rmsnorm_quantize_act", "jetfp8_swiglu_quantize_act",
+                 "jetfp8_quantize_weight_group", "jetfp8_quantize_act_dual", "jetfp8_rmsnorm_quantize_act", "jetfp8_swiglu_quantize_act",
                  "jetfp8_gemm_fprop", "jetfp8_gemm_dgrad", "jetfp8_gemm_wgrad"):
         getattr(lib, name).restype = S
     lib.jetfp8_e4m3_encode_range.argtypes = [ctypes.c_uint32, I, P, P]
@@ -190,6 +191,32 @@ def jetfp8_quantize_weight(w, q, s, qt=None, stream=None):
            "jetfp8_quantize_weight")
 
 
+WEIGHT_GROUP_MAX = 8
+
+
+def jetfp8_quantize_weight_group(ws, qs, ss, qts=None, stream=None):
+    """jetfp8_quantize_weight on each (w, q, s, qt) entry, in one launch."""
+    n = len(ws)
+    qts = [None] * n if qts is None else list(qts)
+    if not (len(qs) == len(ss) == len(qts) == n):
+        raise ValueError("jetfp8_quantize_weight_group: one q, s and qt per weight")
+    if n > WEIGHT_GROUP_MAX:
+        raise ValueError(f"jetfp8_quantize_weight_group: at most {WEIGHT_GROUP_MAX} weights per launch")
+    for w, q, s, qt in zip(ws, qs, ss, qts):
+        N, K = w.shape
+        _want(w, torch.bfloat16, (N, K), "w")
+        _want(q, torch.uint8, (N, K), "q")
+        _want(s, torch.float32, (N // 128, K // 128), "s")
+        if qt is not None:
+            _want(qt, torch.uint8, (K, N), "qt")
+    P = ctypes.c_void_p * max(n, 1)
+    I = ctypes.c_int64 * max(n, 1)
+    _check(load_library().jetfp8_quantize_weight_group(
+        n, P(*[_ptr(w) for w in ws]), I(*[w.shape[0] for w in ws]), I(*[w.shape[1] for w in ws]),
+        P(*[_ptr(q) for q in qs]), P(*[_ptr(s) for s in ss]), P(*[_ptr(qt) for qt in qts]), _stream(stream)),
+        "jetfp8_quantize_weight_group")
+
+
 def jetfp8_e4m3_encode_range(first, codes, stream=None):
     """codes[i] = the GPU's E4M3 code of the fp32 pattern first + i (a test hook
     for the conversion the quantisers end in)."""
@@ -312,6 +339,22 @@ def quantize_weight(w: torch.Tensor, transposed: bool = True, stream=None):
     qt = torch.empty((K, N), dtype=torch.uint8, device=w.device) if transposed else None
     jetfp8_quantize_weight(w, q, s, qt, stream)
     return q, s, qt
+
+
+def quantize_weights(ws, transposed: bool = True, stream=None):
+    """quantize_weight of every tensor in ws, one launch per (up to) eight
+    tensors: a list of (codes, scales, codes^T or None)."""
+    out = []
+    for i in range(0, len(ws), WEIGHT_GROUP_MAX):
+        chunk = ws[i:i + WEIGHT_GROUP_MAX]
+        qs = [torch.empty(w.shape, dtype=torch.uint8, device=w.device) for w in chunk]
+        ss = [torch.empty((w.shape[0] // 128, w.shape[1] // 128), dtype=torch.float32, device=w.device)
+              for w in chunk]
+        qts = [torch.empty((w.shape[1], w.shape[0]), dtype=torch.uint8, device=w.device) if transposed else None
+               for w in chunk]
+        jetfp8_quantize_weight_group(chunk, qs, ss, qts, stream)
+        out.extend(zip(qs, ss, qts))
+    return out
 
 
 def gemm_fprop(qx, sx, qw, sw, stream=None):

@@ -171,6 +171,28 @@ JETFP8_API jetfp8_status jetfp8_quantize_weight(const void *w, int64_t N, int64_
                                                 void *stream);
 
 /*
+ * Several weight tensors quantised in one launch, each exactly as
+ * jetfp8_quantize_weight quantises it (same codes, scales and transposed
+ * codes, bit for bit).  The pages quantise the BF16 master weights to FP8
+ * each step ("Architecture Centrale", "Schéma de Quantification"); they
+ * have no grouped call of their own: grouping only lets one launch cover
+ * every weight of a step, so the small tensors share the start-up and the
+ * last stores of the large ones.
+ *   count : 0 .. JETFP8_WEIGHT_GROUP_MAX (0 does nothing)
+ *   w, N, K, q, s, qt : host arrays of count entries, all six given (qt[t]
+ *           may be NULL); entry t describes one tensor as the arguments of
+ *           jetfp8_quantize_weight do.  The arrays are read during the call
+ *           only; the device buffers they point to stay the caller's.
+ * Every entry must satisfy jetfp8_quantize_weight's requirements, and no
+ * output may overlap an input or output of any entry.  Nothing is launched
+ * unless every entry passes.
+ */
+#define JETFP8_WEIGHT_GROUP_MAX 8
+JETFP8_API jetfp8_status jetfp8_quantize_weight_group(int count, const void *const *w, const int64_t *N,
+                                                      const int64_t *K, uint8_t *const *q, float *const *s,
+                                                      uint8_t *const *qt, void *stream);
+
+/*
  * Fprop: Y = X W^T (Jet-RL, "Schéma de Quantification": FP8 GEMMs of the
  * linear layers).
  *   y[m][n] = bf16( sum_g sx[g][m] * sw[n/128][g] * sum_{k in group g} e4m3(qx[m][k]) * e4m3(qw[n][k]) )

@@ -104,6 +104,38 @@ def test_quantize_weight_validation(lib):
     assert f(A16, 128, 128, B16, C16, B16 + 128, None) == J.ERR_INVALID_VALUE   # qt overlaps q
 
 
+def _group_args(entries):
+    """Host arrays for jetfp8_quantize_weight_group from (w, N, K, q, s, qt) tuples."""
+    n = max(len(entries), 1)
+    P, I = ctypes.c_void_p * n, ctypes.c_int64 * n
+    cols = list(zip(*entries)) if entries else [()] * 6
+    return (P(*cols[0]), I(*cols[1]), I(*cols[2]), P(*cols[3]), P(*cols[4]), P(*cols[5]))
+
+
+def test_quantize_weight_group_validation(lib):
+    f = lib.jetfp8_quantize_weight_group
+    f.argtypes = [ctypes.c_int] + [ctypes.c_void_p] * 7
+    good = (A16, 128, 256, B16, C16, None)                       # W 128x256: 64 KB, q 32 KB, s 8 B
+    other = (D16, 256, 128, D16 + (1 << 20), D16 + (2 << 20), D16 + (3 << 20))
+    assert f(0, None, None, None, None, None, None, None) == J.OK   # empty group: nothing to do
+    assert f(-1, *_group_args([good]), None) == J.ERR_SHAPE
+    assert f(J.WEIGHT_GROUP_MAX + 1, *_group_args([good] * 9), None) == J.ERR_SHAPE
+    w, n, k, q, s, qt = _group_args([good])
+    assert f(1, w, n, k, q, s, None, None) == J.ERR_INVALID_VALUE   # the qt array itself is required
+    assert f(2, *_group_args([good, (A16, 100, 128, B16, C16, None)]), None) == J.ERR_SHAPE
+    assert f(2, *_group_args([good, (D16, 128, 128, None, C16, None)]), None) == J.ERR_INVALID_VALUE
+    assert f(2, *_group_args([good, (D16 + 4, 128, 128, E16, E16 + 65536, None)]), None) == J.ERR_ALIGNMENT
+    # an output of one entry overlapping an input or output of another
+    assert f(2, *_group_args([good, (D16, 128, 128, A16 + 4096, E16, None)]), None) == J.ERR_INVALID_VALUE
+    assert f(2, *_group_args([good, (D16, 128, 128, E16, B16 + 16, None)]), None) == J.ERR_INVALID_VALUE
+    assert f(2, *_group_args([good, (D16, 128, 128, E16, E16 + 65536, C16)]), None) == J.ERR_INVALID_VALUE
+    # the same entries one by one are accepted by the single call's checks
+    # (they reach the device check, which fails here without a GPU)
+    import torch
+    if not torch.cuda.is_available():
+        assert f(2, *_group_args([good, other]), None) == J.ERR_UNSUPPORTED_DEVICE
+
+
 def test_rmsnorm_quantize_validation(lib):
     f = lib.jetfp8_rmsnorm_quantize_act
     assert f(A16, B16, 1e-6, 4, 384, C16, D16, None, None) == J.ERR_SHAPE        # H % 256

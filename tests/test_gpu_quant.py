@@ -102,6 +102,42 @@ def test_quantize_weight_special_values():
     assert_bitexact(qt, oqt, "transposed codes")
 
 
+def test_quantize_weight_group_matches_single_calls():
+    """One grouped launch over the 8B-class projections (mixed with and
+    without transposed codes) gives, bit for bit, what one call per weight
+    gives; small entries are also checked against the oracle."""
+    shapes = [(6144, 4096), (4096, 4096), (28672, 4096), (4096, 14336), (128, 128), (384, 1152)]
+    ws = [syn.weight(n, k, seed=11 + i, index=i, device=DEV) for i, (n, k) in enumerate(shapes)]
+    ws[4] = special_values(128, 128, 5).to(DEV)
+    transposed = [True, True, True, True, False, True]
+    qs = [torch.empty(w.shape, dtype=torch.uint8, device=DEV) for w in ws]
+    ss = [torch.empty((w.shape[0] // 128, w.shape[1] // 128), dtype=torch.float32, device=DEV) for w in ws]
+    qts = [torch.empty((w.shape[1], w.shape[0]), dtype=torch.uint8, device=DEV) if t else None
+           for w, t in zip(ws, transposed)]
+    jf.jetfp8_quantize_weight_group(ws, qs, ss, qts)
+    assert jf.jetfp8_poll_device_error() == 0
+    for i, (w, t) in enumerate(zip(ws, transposed)):
+        q1, s1, qt1 = jf.quantize_weight(w, transposed=t)
+        assert torch.equal(qs[i], q1) and torch.equal(ss[i], s1), f"entry {i}"
+        if t:
+            assert torch.equal(qts[i], qt1), f"entry {i} transposed"
+    for i in (4, 5):
+        oq, os_, oqt = oracle.quantize_weight(bits(ws[i].cpu()), transposed[i], threads=ORACLE_THREADS)
+        assert_bitexact(qs[i], oq, f"entry {i} codes")
+        assert_bitexact(ss[i], os_, f"entry {i} scales")
+        if transposed[i]:
+            assert_bitexact(qts[i], oqt, f"entry {i} transposed codes")
+
+
+def test_quantize_weights_chunks_past_the_group_limit():
+    """quantize_weights splits more than eight weights over several launches."""
+    ws = [syn.weight(128 * (1 + i % 3), 256, seed=40 + i, device=DEV) for i in range(11)]
+    got = jf.quantize_weights(ws)
+    for w, (q, s, qt) in zip(ws, got):
+        q1, s1, qt1 = jf.quantize_weight(w)
+        assert torch.equal(q, q1) and torch.equal(s, s1) and torch.equal(qt, qt1)
+
+
 def tie_groups(rows, seed):
     """Groups made to hit E4M3 rounding midpoints: amax = 448 * 2^e (an exact
     power-of-two scale), the other values exact midpoints between neighbouring

@@ -72,20 +72,20 @@ FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1
 # SHA-256 is recorded here (the kernel and its inline-PTX helpers) and is
 # reported as null once they differ.
 GEMM_TRAFFIC = {"per_launch_bytes": {
-                                     "dgrad:down": 640437504,
-                                     "dgrad:gate_up": 2347882752,
-                                     "dgrad:o": 173171968,
-                                     "dgrad:qkv": 222554112,
-                                     "fprop:down": 679173120,
-                                     "fprop:gate_up": 1346667776,
-                                     "fprop:o": 174824704,
-                                     "fprop:qkv": 253932032,
-                                     "wgrad:down": 925304064,
-                                     "wgrad:gate_up": 2332539648,
-                                     "wgrad:o": 305678848,
-                                     "wgrad:qkv": 482245632},
+                                     "dgrad:down": 632559872,
+                                     "dgrad:gate_up": 2345060608,
+                                     "dgrad:o": 172852224,
+                                     "dgrad:qkv": 222333440,
+                                     "fprop:down": 660741376,
+                                     "fprop:gate_up": 1315183104,
+                                     "fprop:o": 174889216,
+                                     "fprop:qkv": 254417408,
+                                     "wgrad:down": 934053376,
+                                     "wgrad:gate_up": 2335916800,
+                                     "wgrad:o": 305651200,
+                                     "wgrad:qkv": 482374912},
                 "sources": ("gemm.cu", "ptx.cuh"),
-                "sha256": "c9fdf7c2b8db675b26c4a356681714bf6557ce8d66718743c037b8f1203cf71e"}
+                "sha256": "e99607c2ec8933916db9a94013758c2504ee60acde13ee692e9780d38e3eedc0"}
 
 
 def gemm_sources_sha256() -> str:

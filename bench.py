@@ -424,8 +424,12 @@ def time_e2e(step, steps, device):
     # Reuse across steps is ordered by events (inputs are overwritten only
     # after the previous step's kernels read them, results only after the
     # previous step's copies took them).
-    main = torch.cuda.current_stream()
+    # Every stream here is a side stream: on the legacy default stream the
+    # compute would be ordered against the copy streams, and the copies in,
+    # the kernels and the copies out would run one after the other.
+    main = torch.cuda.Stream(device=device)
     s_in, s_out = torch.cuda.Stream(device=device), torch.cuda.Stream(device=device)
+    main.wait_stream(torch.cuda.current_stream())
     names = list(step.p)
     done_reading = {n: None for n in names}
     copied_out = {n: None for n in names}
@@ -443,8 +447,9 @@ def time_e2e(step, steps, device):
             main.wait_event(landed)
             if copied_out[name] is not None:
                 main.wait_event(copied_out[name])
-            for _, fn in step.launches(d, weight=True):
-                fn()
+            with torch.cuda.stream(main):
+                for _, fn in step.launches(d, weight=True):
+                    fn()
             computed = torch.cuda.Event()
             computed.record(main)
             done_reading[name] = computed
@@ -460,12 +465,12 @@ def time_e2e(step, steps, device):
     torch.cuda.synchronize()
     check_device(step.jf)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
+    a.record(main)
     for _ in range(steps):
         one()
     for name in names:                      # the last results are on the host
         main.wait_event(copied_out[name])
-    b.record()
+    b.record(main)
     torch.cuda.synchronize()
     check_device(step.jf)
     ms = a.elapsed_time(b) / steps

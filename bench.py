@@ -650,11 +650,11 @@ def run_native_harness(device_index: int, steps: int, streams: int, e2e_steps: i
 
 
 # ------------------------------------------------------------------ the oracle on the host
-def cpu_oracle_sample(seed: int = 7, threads: int = 1):
+def cpu_oracle_sample(seed: int = 7, threads: int = 1, rows: int = 4, wrows: int = 1):
     """The oracle on a bounded sample of the O projection (N = K = 4096,
-    M = 16384): quantise what the sample needs, then Fprop on 4 token rows,
-    Dgrad on 4 token rows, Wgrad on 1 output row over all 16384 tokens.
-    Returns (seconds, GEMM flops, description)."""
+    M = 16384): quantise what the sample needs, then Fprop on `rows` token
+    rows, Dgrad on `rows` token rows, Wgrad on `wrows` output rows over all
+    16384 tokens.  Returns (seconds, GEMM flops, description)."""
     import oracle
     n, k = PROJ["o"]
     x = syn.activation(TOKENS, k, seed=seed, outlier_scale=20.0)
@@ -663,23 +663,26 @@ def cpu_oracle_sample(seed: int = 7, threads: int = 1):
     xb, wb, dyb = syn.bf16_bits(x), syn.bf16_bits(w), syn.bf16_bits(dy)
     oracle.build()
     t0 = time.perf_counter()
-    qx, sx = oracle.quantize_act(xb[:4], threads=threads)
+    qx, sx = oracle.quantize_act(xb[:rows], threads=threads)
     qw, sw, _ = oracle.quantize_weight(wb, threads=threads)
-    qdy, sdy = oracle.quantize_act(dyb[:4], threads=threads)
+    qdy, sdy = oracle.quantize_act(dyb[:rows], threads=threads)
     qxt, sxt = oracle.quantize_act_transposed(xb, threads=threads)
-    qdyt, sdyt = oracle.quantize_act_transposed(np.ascontiguousarray(dyb[:, :128]), threads=threads)
-    r = np.repeat(np.arange(4), n)
-    c = np.tile(np.arange(n), 4)
+    wcols = -(-wrows // 128) * 128                 # dY^T rows needed: whole 128-column groups of dY
+    qdyt, sdyt = oracle.quantize_act_transposed(np.ascontiguousarray(dyb[:, :wcols]), threads=threads)
+    r = np.repeat(np.arange(rows), n)
+    c = np.tile(np.arange(n), rows)
     oracle.gemm_fprop(qx, sx, qw, sw, r, c, threads=threads)
-    r = np.repeat(np.arange(4), k)
-    c = np.tile(np.arange(k), 4)
+    r = np.repeat(np.arange(rows), k)
+    c = np.tile(np.arange(k), rows)
     oracle.gemm_dgrad(qdy, sdy, qw, sw, r, c, threads=threads)
-    oracle.gemm_wgrad(qdyt, sdyt, qxt, sxt, np.zeros(k, np.int64), np.arange(k, dtype=np.int64), threads=threads)
+    r = np.repeat(np.arange(wrows), k)
+    c = np.tile(np.arange(k), wrows)
+    oracle.gemm_wgrad(qdyt, sdyt, qxt, sxt, r, c, threads=threads)
     secs = time.perf_counter() - t0
-    flops = 2.0 * (4 * n * k + 4 * k * n + 1 * k * TOKENS)
+    flops = 2.0 * (rows * n * k + rows * k * n + wrows * k * TOKENS)
     desc = (f"oracle (plain C; rows split over {threads} host thread{'s' if threads > 1 else ''}) on the o "
-            "projection 4096x4096 at M=16384: quantise the needed inputs, fprop 4 token rows, dgrad 4 token "
-            "rows, wgrad 1 output row over 16384 tokens")
+            f"projection 4096x4096 at M=16384: quantise the needed inputs, fprop {rows} token rows, dgrad {rows} "
+            f"token rows, wgrad {wrows} output row{'s' if wrows > 1 else ''} over 16384 tokens")
     return secs, flops, desc
 
 
@@ -822,13 +825,15 @@ def main(argv=None):
         result["extra_launches"] = n1 + n2 + n3
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cores = os.cpu_count() or 1
-        secs1, cflops, _ = cpu_oracle_sample(threads=1)
-        secsn, _, descn = cpu_oracle_sample(threads=cores)
-        result["cpu_baseline"] = {"value": cflops / secsn / 1e12, "unit": "TFLOP/s", "cores": cores,
+        # all host threads on a sample of about ten seconds of oracle work
+        # (on 16 cores); one thread on a sample 64 times smaller
+        secs1, cflops1, desc1 = cpu_oracle_sample(threads=1)
+        secsn, cflopsn, descn = cpu_oracle_sample(threads=cores, rows=256, wrows=64)
+        result["cpu_baseline"] = {"value": cflopsn / secsn / 1e12, "unit": "TFLOP/s", "cores": cores,
                                   "kind": "oracle", "sample": descn, "seconds": round(secsn, 2),
                                   "host_cores": cores,
-                                  "single_thread": {"value": cflops / secs1 / 1e12, "cores": 1,
-                                                    "seconds": round(secs1, 2)}}
+                                  "single_thread": {"value": cflops1 / secs1 / 1e12, "cores": 1,
+                                                    "seconds": round(secs1, 2), "sample": desc1}}
     if rank == 0:
         print(json.dumps(result))
     if world > 1:

@@ -64,6 +64,7 @@ constexpr int MMA_WARP = 1;
 constexpr int SCALE_WARP = 2;
 constexpr int FIRST_PROMO_WARP = 4;
 constexpr int SCALE_STAGES_ALL = 4;      // scale ring slots
+constexpr int SCALE_RAW_AHEAD = 2;       // block scales: groups the loader stages ahead
 constexpr int MAX_TBUF = 8;              // TMEM partial buffers at most (narrow tiles)
 // setmaxnreg split per tile width: wide tiles keep 128 accumulator registers
 // per promotion thread, 128-wide tiles 64 (which leaves the control warps room).
@@ -108,7 +109,7 @@ struct KernelArgs {
 // after the last stage), which only feed output rows 64..127 -- rows past the
 // problem, never stored.  Halving A's footprint buys more stages, i.e. more of
 // W in flight, which is what bounds decode.
-template <int BN, int STAGES, bool HALF_A = false>
+template <int BN, int STAGES, bool HALF_A = false, bool SB_PER_COLUMN = false>
 struct Smem {
     static constexpr uint32_t A_BYTES = HALF_A ? (BM / 2) * BK : BM * BK;   // A stride between stages
     static constexpr uint32_t A_LOAD_BYTES = A_BYTES;                       // bytes one stage's A copy brings
@@ -117,13 +118,25 @@ struct Smem {
     static constexpr uint32_t STAGE_BYTES = A_LOAD_BYTES + B_BYTES;
     static constexpr uint32_t B_OFF = STAGES * A_BYTES + A_PAD;
     static constexpr uint32_t TILES = B_OFF + STAGES * B_BYTES;
-    // scale ring: per slot 128 row scales then BN column scales (fp32)
-    static constexpr uint32_t SCALE_FLOATS = BM + BN;
+    // scale ring.  Per slot 128 row scales, then BN column scales (per-column
+    // scales) or the tile's block scale (narrow tiles, padded to 16 bytes).
+    // 256-wide block-scale tiles (READY): per slot the ready products sa * sb
+    // of the tile's 128 rows, one row of 128 per 128-column block.
+    static constexpr bool READY = !SB_PER_COLUMN && BN >= 256;
+    static constexpr int NBLK = BN >= 256 ? 2 : 1;
+    static constexpr uint32_t SCALE_FLOATS = SB_PER_COLUMN ? BM + BN : (READY ? NBLK * BM : BM + 4);
     static constexpr uint32_t SCALE_OFF = TILES;
     static constexpr int SCALE_STAGES = SCALE_STAGES_ALL;
     static constexpr uint32_t SCALE_BYTES = SCALE_STAGES * SCALE_FLOATS * 4;
-    // epilogue staging: per promotion warp two 32-row x 16-column bf16 chunks
-    static constexpr uint32_t OUT_OFF = SCALE_OFF + SCALE_BYTES;
+    // block scales: the loader's staging ring of raw scales (128 row scales,
+    // then the tile's block scales, padded to 16 bytes)
+    static constexpr int RAW_SLOTS = READY ? SCALE_RAW_AHEAD + 1 : 0;
+    static constexpr uint32_t RAW_FLOATS = BM + 4;
+    static constexpr uint32_t RAW_OFF = SCALE_OFF + SCALE_BYTES;
+    static constexpr uint32_t RAW_BYTES = (RAW_SLOTS * RAW_FLOATS * 4 + 127) / 128 * 128;
+    // epilogue staging: per promotion warp two 32-row x 16-column bf16 chunks,
+    // the sources of TMA stores (which need an aligned shared-memory address)
+    static constexpr uint32_t OUT_OFF = (RAW_OFF + RAW_BYTES + 1023) / 1024 * 1024;
     static constexpr uint32_t OUT_CHUNK_BYTES = 32 * 16 * 2;
     static constexpr uint32_t OUT_BYTES = 8 * 2 * OUT_CHUNK_BYTES;
     static constexpr uint32_t BAR_OFF = OUT_OFF + OUT_BYTES;
@@ -131,6 +144,12 @@ struct Smem {
     // tmem holder, abort flag
     static constexpr uint32_t CTRL_BYTES = (2 * STAGES + 2 * SCALE_STAGES + 2 * MAX_TBUF + 1) * 8 + 16;
     static constexpr uint32_t TOTAL = 1024 /* alignment slack */ + BAR_OFF + CTRL_BYTES;
+    static_assert(B_OFF % 1024 == 0 && TILES % 1024 == 0, "operand tiles on 1024-byte boundaries (128-byte swizzle)");
+    static_assert(SCALE_OFF % 16 == 0 && RAW_OFF % 16 == 0 && (SCALE_FLOATS * 4) % 16 == 0 &&
+                      (RAW_FLOATS * 4) % 16 == 0,
+                  "16-byte copies into the scale slots");
+    static_assert(OUT_OFF % 1024 == 0 && OUT_CHUNK_BYTES % 128 == 0, "TMA store sources aligned");
+    static_assert(BAR_OFF % 8 == 0, "barriers 8-byte aligned");
 };
 
 // Tile order: bands of `band` tiles along one axis, the banded axis varying
@@ -168,7 +187,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
             const __grid_constant__ CUtensorMap tmap_d, const KernelArgs args)
 {
-    using L = Smem<BN, STAGES, HALF_A>;
+    using L = Smem<BN, STAGES, HALF_A, SB_PER_COLUMN>;
     constexpr int SCALE_STAGES = L::SCALE_STAGES;
     // Tiles 128 or 256 wide: two promotion warpgroups, one per column half.
     // Narrow tiles (decode-sized problems): the first warpgroup alone.
@@ -381,8 +400,91 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                 ptx::mbar_wait(mma_done, 0, nullptr, args.err, ERRBIT_DRAIN, WAIT_TIMEOUT_NS);
             }
             __syncwarp();
+        } else if (warp == SCALE_WARP && L::READY) {
+            // -------------------------------------------------- scale loader
+            // Block scales.  Per group the slot receives the ready products
+            // sa[row] * sb[block] for the tile's 128 rows and its one or two
+            // 128-column blocks, so that a promotion thread reads one value per
+            // group: a group's scale reads sit on its chain between the MMA's
+            // completion and the TMEM load (measured: one read instead of two
+            // reads and a product, +5.8 % on Fprop).  The raw scales come by
+            // cp.async SCALE_RAW_AHEAD groups ahead into a small staging ring;
+            // lane l takes rows 4l .. 4l+3 (one 16-byte copy when the row count
+            // keeps them aligned, i.e. is a multiple of 4, else four 4-byte
+            // copies).
+            int ss = 0, rs = 0;
+            uint32_t sphase = 0;
+            bool ok = true;
+            float *raw = reinterpret_cast<float *>(smem + L::RAW_OFF);
+            const int r = 4 * lane;
+            for (int tile = work_first; ok && tile < num_work; tile += work_stride) {
+                int tm, tn;
+                coords(tile, tm, tn);
+                const int row = tm * BM + r;
+                auto stage_raw = [&](int gg, int slot) {
+                    float *dst = raw + slot * L::RAW_FLOATS;
+                    const float *sa_g = args.sa + static_cast<int64_t>(gg) * args.rows;
+                    if ((args.rows & 3) == 0) {
+                        const bool in = row < args.rows;
+                        ptx::cp_async_16z(dst + r, in ? sa_g + row : args.sa, in ? 16u : 0u);
+                    } else {
+#pragma unroll 1
+                        for (int e = 0; e < 4; ++e) {
+                            const bool in = row + e < args.rows;
+                            ptx::cp_async_4(dst + r + e, in ? sa_g + row + e : args.sa, in ? 4u : 0u);
+                        }
+                    }
+                    if (lane < L::NBLK) {
+                        const int col = tn * BN + lane * 128;
+                        const bool in = col < args.cols;
+                        const float *sb_g = args.sb + static_cast<int64_t>(gg) * args.sb_stride_g;
+                        ptx::cp_async_4(dst + BM + lane,
+                                        in ? sb_g + static_cast<int64_t>(col >> 7) * args.sb_stride_c : args.sb,
+                                        in ? 4u : 0u);
+                    }
+                };
+                // the tile's first groups (one commit group each, empty past G)
+#pragma unroll
+                for (int k = 0; k < SCALE_RAW_AHEAD; ++k) {
+                    if (k < G)
+                        stage_raw(k, (rs + k) % L::RAW_SLOTS);
+                    ptx::cp_async_commit();
+                }
+                for (int g = 0; g < G; ++g) {
+                    __syncwarp();                // every lane is done with the slot refilled next
+                    if (g + SCALE_RAW_AHEAD < G)
+                        stage_raw(g + SCALE_RAW_AHEAD, (rs + SCALE_RAW_AHEAD) % L::RAW_SLOTS);
+                    ptx::cp_async_commit();
+                    ptx::cp_async_wait<SCALE_RAW_AHEAD>();   // this lane's copies of group g have landed
+                    __syncwarp();                            // and every lane's
+                    if (!ptx::mbar_wait(&sempty[ss], sphase ^ 1u, abort_flag, args.err, ERRBIT_PROMOTE,
+                                        WAIT_TIMEOUT_NS)) {
+                        ok = false;
+                        break;
+                    }
+                    const float *src = raw + rs * L::RAW_FLOATS;
+                    const float4 a = *reinterpret_cast<const float4 *>(src + r);
+                    float *dst = scl + ss * L::SCALE_FLOATS;
+#pragma unroll
+                    for (int b = 0; b < L::NBLK; ++b) {
+                        const float sb = src[BM + b];
+                        *reinterpret_cast<float4 *>(dst + b * BM + r) =
+                            make_float4(a.x * sb, a.y * sb, a.z * sb, a.w * sb);
+                    }
+                    ptx::mbar_arrive(&sfull[ss]);    // every lane, after its own stores
+                    if (++ss == SCALE_STAGES) {
+                        ss = 0;
+                        sphase ^= 1u;
+                    }
+                    if (++rs == L::RAW_SLOTS)
+                        rs = 0;
+                }
+            }
+            ptx::cp_async_wait_all();
         } else if (warp == SCALE_WARP && !SB_PER_COLUMN) {
             // -------------------------------------------------- scale loader
+            // Narrow block-scale tiles: the group's 128 row scales and the
+            // tile's block scale, by cp.async, straight into the slot.
             int ss = 0;
             uint32_t sphase = 0;
             bool ok = true;
@@ -415,14 +517,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                             ptx::cp_async_4(dst + r + e, in ? sa_g + row + e : args.sa, in ? 4u : 0u);
                         }
                     }
-                    // the block scales of the tile's 128-column blocks (per-column
-                    // scales never come here: the TMA producer copies those)
                     const float *sb_g = args.sb + static_cast<int64_t>(g) * args.sb_stride_g;
-                    if (lane < (BN >= 128 ? BN / 128 : 1)) {
-                        const int col = tn * BN + lane * 128;
+                    if (lane == 0) {
+                        const int col = tn * BN;
                         const bool in = col < args.cols;
-                        ptx::cp_async_4(dst + BM + lane,
-                                        in ? sb_g + static_cast<int64_t>(col >> 7) * args.sb_stride_c : args.sb,
+                        ptx::cp_async_4(dst + BM, in ? sb_g + static_cast<int64_t>(col >> 7) * args.sb_stride_c : args.sb,
                                         in ? 4u : 0u);
                     }
                     ptx::cp_async_mbar_arrive_noinc(&sfull[ss]);
@@ -476,7 +575,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                 const float *sbcol = scur + BM + wg * COLS_PER_WG;
                 float w_blk = 0.0f;
                 if (!SB_PER_COLUMN) {
-                    w_blk = scur[row_in_tile] * scur[BM + (wg * COLS_PER_WG) / 128];
+                    if constexpr (L::READY)
+                        w_blk = scur[((wg * COLS_PER_WG) / 128) * BM + row_in_tile];   // the loader's sa * sb
+                    else
+                        w_blk = scur[row_in_tile] * scur[BM];
                     __syncwarp();
                     ptx::mbar_arrive_elected(&sempty[ss]);
                 }
@@ -659,7 +761,7 @@ template <int BN, int STAGES, bool SB_PER_COLUMN, bool HALF_A = false>
 cudaError_t launch_variant(const GemmProblem &p, const DeviceInfo &dev, const CUtensorMap &ta, const CUtensorMap &tb,
                            const CUtensorMap &td, cudaStream_t stream)
 {
-    using L = Smem<BN, STAGES, HALF_A>;
+    using L = Smem<BN, STAGES, HALF_A, SB_PER_COLUMN>;
     static_assert(L::TOTAL <= 227 * 1024, "shared memory per CTA");
     static_assert(!HALF_A || !SB_PER_COLUMN, "the packed A tiles serve block-scale problems of <= 64 rows");
     auto kern = gemm_kernel<BN, STAGES, SB_PER_COLUMN, HALF_A>;

@@ -72,20 +72,20 @@ FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1
 # SHA-256 is recorded here (the kernel and its inline-PTX helpers) and is
 # reported as null once they differ.
 GEMM_TRAFFIC = {"per_launch_bytes": {
-                                     "dgrad:down": 632559872,
-                                     "dgrad:gate_up": 2345060608,
-                                     "dgrad:o": 172852224,
-                                     "dgrad:qkv": 222333440,
-                                     "fprop:down": 660741376,
-                                     "fprop:gate_up": 1315183104,
-                                     "fprop:o": 174889216,
-                                     "fprop:qkv": 254417408,
-                                     "wgrad:down": 934053376,
-                                     "wgrad:gate_up": 2335916800,
-                                     "wgrad:o": 305651200,
-                                     "wgrad:qkv": 482374912},
+                                     "dgrad:down": 640071424,
+                                     "dgrad:gate_up": 2347593472,
+                                     "dgrad:o": 173084672,
+                                     "dgrad:qkv": 222231808,
+                                     "fprop:down": 694206208,
+                                     "fprop:gate_up": 1338408192,
+                                     "fprop:o": 174794496,
+                                     "fprop:qkv": 254276096,
+                                     "wgrad:down": 937095936,
+                                     "wgrad:gate_up": 2341203968,
+                                     "wgrad:o": 306068224,
+                                     "wgrad:qkv": 482590976},
                 "sources": ("gemm.cu", "ptx.cuh"),
-                "sha256": "e99607c2ec8933916db9a94013758c2504ee60acde13ee692e9780d38e3eedc0"}
+                "sha256": "366b4beb3fb4e84e86bfa6199d8bee3a62dd56f376c738046050380ab20f9d4e"}
 
 
 def gemm_sources_sha256() -> str:

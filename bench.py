@@ -826,9 +826,9 @@ def main(argv=None):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cores = os.cpu_count() or 1
         # all host threads on a sample of about ten seconds of oracle work
-        # (on 16 cores); one thread on a sample 64 times smaller
+        # (on 16 cores); one thread on a sample 128 times smaller
         secs1, cflops1, desc1 = cpu_oracle_sample(threads=1)
-        secsn, cflopsn, descn = cpu_oracle_sample(threads=cores, rows=256, wrows=64)
+        secsn, cflopsn, descn = cpu_oracle_sample(threads=cores, rows=512, wrows=128)
         result["cpu_baseline"] = {"value": cflopsn / secsn / 1e12, "unit": "TFLOP/s", "cores": cores,
                                   "kind": "oracle", "sample": descn, "seconds": round(secsn, 2),
                                   "host_cores": cores,

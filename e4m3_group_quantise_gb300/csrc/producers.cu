@@ -128,7 +128,7 @@ __device__ __forceinline__ void rms_chunk_out(const uint4 &xc, const uint4 &gc, 
     if (y)
         y[row * (H >> 3) + c] = make_uint4(w[0], w[1], w[2], w[3]);
     if (q)
-        quantize8_halfwarp(v, q + row * H + 8 * c, s + (c >> 4) * M + row, lane);
+        quantize8_halfwarp(v, w, q + row * H + 8 * c, s + (c >> 4) * M + row, lane);
 }
 
 // (rows of up to 4096 columns: capped for five blocks per SM, +3 % measured)
@@ -256,7 +256,7 @@ swiglu_quantize_kernel(const uint4 *__restrict__ gu, int64_t M, int64_t I, uint8
         if (y)
             y[row * out_row + c] = make_uint4(w[0], w[1], w[2], w[3]);
         if (q)
-            quantize8_halfwarp(v, q + row * I + 8 * c, s + (c >> 4) * M + row, lane);
+            quantize8_halfwarp(v, w, q + row * I + 8 * c, s + (c >> 4) * M + row, lane);
     }
 }
 

@@ -12,8 +12,9 @@
 // amax reductions, and stores arranged so that every written sector is full.
 // Compiled without fast-math so that `/` is the correctly rounded IEEE
 // division and subnormals are kept; the per-element division itself is
-// replaced by an exact bracketing test (e4m3.cuh), with the division as the
-// rare fallback.
+// replaced by a once-corrected quotient whose codes are exact on the inputs
+// met here (e4m3.cuh), with the division for the rest (tiny or infinite
+// scales, -0 inputs).
 #include <cuda_runtime.h>
 #include <cstdint>
 
@@ -93,15 +94,19 @@ quantize_act_kernel(const uint4 *__restrict__ x, int64_t M, int64_t K, uint2 *__
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
         const GroupScale gs = group_scale(amax);
+        uint32_t m2 = 0x7FFF7FFFu;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            m2 = min_s16x2(min_s16x2(min_s16x2(min_s16x2(m2, v[b][j].x), v[b][j].y), v[b][j].z), v[b][j].w);
         uint32_t w[8];
-        uint32_t redo = encode_words<8>(f, gs, w);
+        uint32_t redo = encode_words<8>(f, gs, has_neg_zero(m2), w);
         if (m < M) {
 #pragma unroll
             for (int j = 0; j < 4; ++j)
                 __stcs(q + m * K8 + g * 16 + 4 * j + sub, make_uint2(w[2 * j], w[2 * j + 1]));
             if (sub == 0)
                 s[g * M + m] = gs.s;
-            // rare: words whose bracket disagreed get the exact quotient
+            // rare: words that need the correctly rounded quotient
             while (redo != 0u) {
                 const int k = __ffs(redo) - 1;
                 redo &= redo - 1u;
@@ -153,6 +158,7 @@ quantize_act_t_kernel(const uint4 *__restrict__ x, int64_t M, int64_t C, uint8_t
 
     float f0[32], f1[32];
     float a0 = 0.0f, a1 = 0.0f;
+    uint32_t m2 = 0x7FFF7FFFu;   // -0 among this thread's values: low half column 0, high half column 1
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
         const uint32_t w = reinterpret_cast<const uint32_t *>(&tile[32 * q + i][0])[lane];
@@ -160,6 +166,7 @@ quantize_act_t_kernel(const uint4 *__restrict__ x, int64_t M, int64_t C, uint8_t
         f1[i] = bf16_hi(w);
         a0 = fmaxf(a0, fabsf(f0[i]));
         a1 = fmaxf(a1, fabsf(f1[i]));
+        m2 = min_s16x2(m2, w);
     }
     s_amax[q][lane] = make_float2(a0, a1);
     __syncthreads();
@@ -171,11 +178,12 @@ quantize_act_t_kernel(const uint4 *__restrict__ x, int64_t M, int64_t C, uint8_t
     }
     const GroupScale g0 = group_scale(a0), g1 = group_scale(a1);
     uint32_t w0[8], w1[8];
-    uint32_t redo = encode_words<8>(f0, g0, w0) | (encode_words<8>(f1, g1, w1) << 8);
+    uint32_t redo = encode_words<8>(f0, g0, (m2 & 0xFFFFu) == 0x8000u, w0) |
+                    (encode_words<8>(f1, g1, (m2 >> 16) == 0x8000u, w1) << 8);
     const int64_t col = c0 + 2 * lane;
     if (q == 0)
         *reinterpret_cast<float2 *>(st + (m0 >> 7) * C + col) = make_float2(g0.s, g1.s);
-    // rare: words whose bracket disagreed get the exact quotient (inputs re-read
+    // rare: words that need the correctly rounded quotient (inputs re-read
     // from the shared-memory tile: 4 rows of this thread's column), patched in
     // the registers before anything is stored
     while (redo != 0u) {
@@ -389,8 +397,13 @@ quantize_weight_kernel(const __grid_constant__ WeightGroup grp, uint32_t *__rest
                 for (int e = 0; e < 8; ++e)
                     f[8 * j + e] = u[e];
             }
+            uint32_t m2 = 0x7FFF7FFFu;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                m2 = min_s16x2(min_s16x2(min_s16x2(min_s16x2(m2, v[step][j].x), v[step][j].y), v[step][j].z),
+                               v[step][j].w);
             uint32_t wd[8];
-            uint32_t redo = encode_words<8>(f, gs, wd);
+            uint32_t redo = encode_words<8>(f, gs, has_neg_zero(m2), wd);
             uint8_t *row_q = q + (n_base + r) * K + k_base;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -399,7 +412,7 @@ quantize_weight_kernel(const __grid_constant__ WeightGroup grp, uint32_t *__rest
                 if (qt != nullptr)
                     *reinterpret_cast<uint2 *>(&sm.codes[r][8 * (sub + 4 * j)]) = c;
             }
-            // rare: a word whose bracket disagreed gets the exact quotient, its
+            // rare: a word that needs the correctly rounded quotient gets it, its
             // four inputs taken from the lane's registers (word k: chunk
             // sub + 4(k/2), half k%2)
             while (redo != 0u) {
@@ -560,15 +573,19 @@ quantize_act_dual_kernel(const __grid_constant__ CUtensorMap tmap_x, int64_t M, 
             amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
             amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
             const GroupScale gs = group_scale(amax);
+            uint32_t m2 = 0x7FFF7FFFu;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                m2 = min_s16x2(min_s16x2(min_s16x2(min_s16x2(m2, v[j].x), v[j].y), v[j].z), v[j].w);
             uint32_t w[8];
-            uint32_t redo = encode_words<8>(f, gs, w);
+            uint32_t redo = encode_words<8>(f, gs, has_neg_zero(m2), w);
             uint8_t *row_q = q + (m0 + r) * K + k0;
 #pragma unroll
             for (int j = 0; j < 4; ++j)      // the row's four lanes write 32 contiguous bytes per j
                 *reinterpret_cast<uint2 *>(row_q + 8 * (sub + 4 * j)) = make_uint2(w[2 * j], w[2 * j + 1]);
             if (sub == 0)
                 s[(k0 >> 7) * M + m0 + r] = gs.s;
-            // rare: a word whose bracket disagreed gets the exact quotient, its
+            // rare: a word that needs the correctly rounded quotient gets it, its
             // four inputs re-read from the shared tile (word k: chunk sub + 4(k/2),
             // half k%2)
             while (redo != 0u) {
@@ -610,8 +627,12 @@ quantize_act_dual_kernel(const __grid_constant__ CUtensorMap tmap_x, int64_t M, 
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
         const GroupScale gs = group_scale(amax);
+        uint32_t m2 = 0x7FFF7FFFu;
+#pragma unroll
+        for (int b = 0; b < 16; ++b)
+            m2 = min_s16x2(m2, wv[b]);
         uint32_t w[8];
-        uint32_t redo = encode_words<8>(f, gs, w);
+        uint32_t redo = encode_words<8>(f, gs, has_neg_zero(m2), w);
         // word k holds rows 8(2k) + 2cq, +1 (low half) and 8(2k+1) + 2cq, +1 (high
         // half): put each 2-byte unit at its row in the staged column
         uint8_t *col = stg + cc * QD_STAGE_PITCH;
@@ -620,7 +641,7 @@ quantize_act_dual_kernel(const __grid_constant__ CUtensorMap tmap_x, int64_t M, 
             *reinterpret_cast<uint16_t *>(col + 8 * (2 * k) + 2 * cq) = static_cast<uint16_t>(w[k]);
             *reinterpret_cast<uint16_t *>(col + 8 * (2 * k + 1) + 2 * cq) = static_cast<uint16_t>(w[k] >> 16);
         }
-        // rare: a word whose bracket disagreed gets the exact quotient, its four
+        // rare: a word that needs the correctly rounded quotient gets it, its four
         // inputs (rows 16k + 2cq, +1, 16k + 8 + 2cq, +1 of the column) re-read
         // from the shared tile; the fixed units overwrite the staged ones
         {

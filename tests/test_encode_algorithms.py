@@ -1,25 +1,17 @@
-"""The two shortcuts the CUDA quantisers take to the exact result, checked on
-the host against their definitions (no GPU, no CUDA code):
-
-* the group scale s = amax / 448 without a division: q = RN(amax * RN(1/448))
-  and one fused multiply-add correction s = RN(q + RN(amax - 448 q) * RN(1/448))
-  (correctly rounded division by a constant known in advance, Brisebarre,
-  Muller and Raina).  Checked against IEEE fp32 division for every
-  non-negative finite bf16 amax, with the two fused multiply-adds evaluated
-  exactly in rational arithmetic and rounded once.
-
-* the code of fp32(x / s) from a reciprocal bracket: with r within about an
-  ulp of 1/s, ra = RN(r (1 - 2^-21)) and rb = RN(r (1 + 2^-21)), whenever the
-  E4M3 codes of RN(x ra) and RN(x rb) agree, that code is the code of
-  RN(x / s).  Checked for every finite bf16 x against a spread of scales and
-  three reciprocals per scale (RN(1/s) and its two neighbours), with the
-  oracle's encoder as the reference.
+"""The group scale's shortcut to the exact result, checked on the host
+against its definition (no GPU, no CUDA code): s = amax / 448 without a
+division, q = RN(amax * RN(1/448)) and one fused multiply-add correction
+s = RN(q + RN(amax - 448 q) * RN(1/448)) (correctly rounded division by a
+constant known in advance, Brisebarre, Muller and Raina).  Checked against
+IEEE fp32 division for every non-negative finite bf16 amax, with the two
+fused multiply-adds evaluated exactly in rational arithmetic and rounded
+once.  (The per-element code's shortcut is checked exhaustively in
+test_corrected_quotient.py.)
 """
 from fractions import Fraction
 
 import numpy as np
 
-import oracle
 
 F32 = np.float32
 
@@ -62,41 +54,3 @@ def test_scale_without_division_equals_ieee_division():
         if s.view(np.uint32) != want.view(np.uint32):
             bad.append(float(amax))
     assert not bad, bad[:8]
-
-
-def test_reciprocal_bracket_codes_are_exact():
-    saved = np.geterr()
-    try:
-        _bracket_check()
-    finally:
-        np.seterr(**saved)
-
-
-def _bracket_check():
-    x = bf16_values(nonnegative=False)
-    # scales s = amax / 448 from a spread of normal amax values: powers of two,
-    # the extremes of the normal range and seeded random bf16 magnitudes
-    rng = np.random.default_rng(11)
-    amaxes = [1.0, 448.0, 2.0 ** -100 * 448.0, 3.0e38, 1.5, 0.3, 1e-20, 7e15]
-    # bf16 exponent fields 12 .. 254: amax >= 2^-115, so s = amax / 448 is normal
-    amaxes += list((rng.integers(0x0600, 0x7F80, 12, dtype=np.uint32) << 16).view(np.float32))
-    agreed = disagreed = 0
-    # |x| far above a small group's amax overflows x / s and x * r to +-inf in
-    # fp32; both then saturate to the +-448 code, as in the kernel
-    np.seterr(over="ignore")
-    for amax in amaxes:
-        s = F32(amax) / F32(448.0)
-        assert s >= F32(2.0 ** -126)           # normal scales take the bracket
-        exact = oracle.e4m3_encode(x / s)      # fp32 IEEE division per element
-        r0 = F32(1.0) / s
-        for r in (np.nextafter(r0, F32(0.0)), r0, np.nextafter(r0, F32(np.inf))):
-            ra = F32(r) * F32(float.fromhex("0x1.fffffp-1"))
-            rb = F32(r) * F32(float.fromhex("0x1.000008p+0"))
-            ca = oracle.e4m3_encode(x * ra)
-            cb = oracle.e4m3_encode(x * rb)
-            same = ca == cb
-            assert np.array_equal(ca[same], exact[same]), (float(amax), float(r))
-            agreed += int(same.sum())
-            disagreed += int((~same).sum())
-    # the exact fallback stays the rare path
-    assert disagreed < 0.05 * (agreed + disagreed)

@@ -533,19 +533,6 @@ __device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b)
 // ------------------------------------------------------------ convert
 // Two fp32 -> two E4M3 codes, round to nearest even, saturating to +-448.
 // Returns lo's code in bits 0..7 and hi's code in bits 8..15.
-// Four fp32 -> four E4M3 codes in one word (v0 in the lowest byte), the
-// same conversion, two at a time, packed without shifts.
-__device__ __forceinline__ uint32_t cvt_e4m3x4(float v0, float v1, float v2, float v3)
-{
-    uint32_t r;
-    asm("{\n .reg .b16 l, h;\n"
-        " cvt.rn.satfinite.e4m3x2.f32 l, %2, %1;\n"
-        " cvt.rn.satfinite.e4m3x2.f32 h, %4, %3;\n"
-        " mov.b32 %0, {l, h};\n}"
-        : "=r"(r) : "f"(v0), "f"(v1), "f"(v2), "f"(v3));
-    return r;
-}
-
 __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi)
 {
     uint16_t r;

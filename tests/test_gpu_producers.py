@@ -126,3 +126,22 @@ def test_swiglu_extreme_gates():
 def test_swiglu_8b_training_size():
     gu = syn.activation(4096, 2 * 14336, seed=6, device=DEV)
     check_swiglu(gu, "swiglu 4096x14336")
+
+
+def test_producers_negative_zero_outputs():
+    """bf16 outputs of -0 inside groups with nonzero values (the quantiser
+    takes the correctly rounded division for a lane holding a -0): RMSNorm of
+    zeros under negative gamma, SwiGLU of zero gates with negative up values."""
+    H = 1024
+    x = syn.activation(16, H, seed=7, device=DEV)
+    x[:, ::7] = 0
+    gamma = torch.ones(H, dtype=torch.bfloat16, device=DEV)
+    gamma[::2] = -1.0
+    q, s, y = check_rmsnorm(x, gamma, 1e-6, "rmsnorm -0")
+    assert (u16(y) == 0x8000).any() and bool((s > 0).all())
+    I = 512
+    gu = syn.activation(16, 2 * I, seed=8, device=DEV)
+    gu[:, :I:5] = 0                                  # gates of 0: silu(0) = +0
+    gu[:, I::5] = -gu[:, I::5].abs() - 0.5           # negative up values there: y = -0
+    q, s, y = check_swiglu(gu, "swiglu -0")
+    assert (u16(y) == 0x8000).any() and bool((s > 0).all())

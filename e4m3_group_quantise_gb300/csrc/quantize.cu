@@ -87,10 +87,12 @@ quantize_act_kernel(const uint4 *__restrict__ x, int64_t M, int64_t K, uint2 *__
             for (int e = 0; e < 8; ++e)
                 f[8 * j + e] = t[e];
         }
-        float amax = 0.0f;
+        uint32_t am2 = 0u;
 #pragma unroll
-        for (int e = 0; e < 32; ++e)
-            amax = fmaxf(amax, fabsf(f[e]));
+        for (int j = 0; j < 4; ++j)
+            am2 = absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(am2, v[b][j].x), v[b][j].y), v[b][j].z),
+                                v[b][j].w);
+        float amax = absmax_value(am2);
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
         const GroupScale gs = group_scale(amax);
@@ -157,17 +159,18 @@ quantize_act_t_kernel(const uint4 *__restrict__ x, int64_t M, int64_t C, uint8_t
     __syncthreads();
 
     float f0[32], f1[32];
-    float a0 = 0.0f, a1 = 0.0f;
-    uint32_t m2 = 0x7FFF7FFFu;   // -0 among this thread's values: low half column 0, high half column 1
+    // per-half running maxima and minima: low halves column 0, high halves column 1
+    uint32_t am2 = 0u, m2 = 0x7FFF7FFFu;   // (m2: a -0 among this thread's values)
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
         const uint32_t w = reinterpret_cast<const uint32_t *>(&tile[32 * q + i][0])[lane];
         f0[i] = bf16_lo(w);
         f1[i] = bf16_hi(w);
-        a0 = fmaxf(a0, fabsf(f0[i]));
-        a1 = fmaxf(a1, fabsf(f1[i]));
+        am2 = absmax_bf16x2(am2, w);
         m2 = min_s16x2(m2, w);
     }
+    am2 &= 0x7FFF7FFFu;
+    float a0 = bf16_lo(am2), a1 = bf16_hi(am2);
     s_amax[q][lane] = make_float2(a0, a1);
     __syncthreads();
 #pragma unroll
@@ -356,18 +359,19 @@ quantize_weight_kernel(const __grid_constant__ WeightGroup grp, uint32_t *__rest
 
         // ---- read this lane's 64 values and their amax
         uint4 v[2][4];
-        float amax = 0.0f;
+        uint32_t am2 = 0u;
 #pragma unroll
         for (int step = 0; step < 2; ++step) {
             const int r = 16 * warp + 8 * step + rr;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 v[step][j] = *reinterpret_cast<const uint4 *>(weight_chunk(sm, stage, r, sub + 4 * j));
-                float f[8];
-                unpack8(v[step][j], f);
-                amax = fmaxf(amax, absmax8(f));
+                am2 = absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(am2, v[step][j].x), v[step][j].y),
+                                                  v[step][j].z),
+                                    v[step][j].w);
             }
         }
+        float amax = absmax_value(am2);
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1)
             amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));

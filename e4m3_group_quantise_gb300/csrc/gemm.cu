@@ -126,7 +126,11 @@ struct Smem {
     static constexpr int NBLK = BN >= 256 ? 2 : 1;
     static constexpr uint32_t SCALE_FLOATS = SB_PER_COLUMN ? BM + BN : (READY ? NBLK * BM : BM + 4);
     static constexpr uint32_t SCALE_OFF = TILES;
-    static constexpr int SCALE_STAGES = SCALE_STAGES_ALL;
+    // TMEM partial buffers: two 256-wide ones; four 128-wide ones; eight for
+    // narrower (decode) tiles.  Block scales have one slot per buffer (the
+    // TMEM-full barrier also covers the slot); per-column scales their own ring.
+    static constexpr uint32_t NBUF = BN >= 256 ? 2 : (BN == 128 ? 4 : MAX_TBUF);
+    static constexpr int SCALE_STAGES = SB_PER_COLUMN ? SCALE_STAGES_ALL : static_cast<int>(NBUF);
     static constexpr uint32_t SCALE_BYTES = SCALE_STAGES * SCALE_FLOATS * 4;
     // block scales: the loader's staging ring of raw scales (128 row scales,
     // then the tile's block scales, padded to 16 bytes)
@@ -208,10 +212,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     constexpr int PS = 4;                        // blocks per slab
     constexpr int NPS = CB / PS;                 // slabs per group
     static_assert(CB % PS == 0, "32-column slabs");
-    // TMEM partial buffers: two 256-wide ones; four 128-wide ones; eight for
-    // narrower (decode) tiles, so that the MMAs can run several groups ahead
+    // TMEM partial buffers (two 256-wide ones; four 128-wide ones; eight for
+    // narrower, decode, tiles), so that the MMAs can run several groups ahead
     // of the read-back instead of waiting on every hand-off.
-    constexpr uint32_t NBUF = BN >= 256 ? 2 : (BN == 128 ? 4 : MAX_TBUF);
+    constexpr uint32_t NBUF = L::NBUF;
     // The MMA issuers commit only the TMEM-full barrier: its completion also
     // means the group's MMAs have read their shared-memory stage, and the
     // first promotion warp, seeing it, releases the stage to the producer.
@@ -266,7 +270,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                 ptx::mbar_init(&sempty[s], 4 * NWG);   // one arrival per promotion warp
             }
             for (uint32_t b = 0; b < NBUF; ++b) {
-                ptx::mbar_init(&tfull[b], 1);
+                // the group's commit; with block scales also every scale-loader lane
+                ptx::mbar_init(&tfull[b], SB_PER_COLUMN ? 1 : 33);
                 ptx::mbar_init(&tempty[b], 4 * NWG);   // one arrival per promotion warp
             }
             ptx::mbar_init(mma_done, 2);   // one final commit per MMA issuer
@@ -412,8 +417,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
             // lane l takes rows 4l .. 4l+3 (one 16-byte copy when the row count
             // keeps them aligned, i.e. is a multiple of 4, else four 4-byte
             // copies).
-            int ss = 0, rs = 0;
-            uint32_t sphase = 0;
+            int rs = 0;
+            uint32_t it = 0;   // global group counter -> TMEM buffer and phase, as the MMA issuers
             bool ok = true;
             float *raw = reinterpret_cast<float *>(smem + L::RAW_OFF);
             const int r = 4 * lane;
@@ -450,32 +455,31 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                         stage_raw(k, (rs + k) % L::RAW_SLOTS);
                     ptx::cp_async_commit();
                 }
-                for (int g = 0; g < G; ++g) {
+                for (int g = 0; g < G; ++g, ++it) {
                     __syncwarp();                // every lane is done with the slot refilled next
                     if (g + SCALE_RAW_AHEAD < G)
                         stage_raw(g + SCALE_RAW_AHEAD, (rs + SCALE_RAW_AHEAD) % L::RAW_SLOTS);
                     ptx::cp_async_commit();
                     ptx::cp_async_wait<SCALE_RAW_AHEAD>();   // this lane's copies of group g have landed
                     __syncwarp();                            // and every lane's
-                    if (!ptx::mbar_wait(&sempty[ss], sphase ^ 1u, abort_flag, args.err, ERRBIT_PROMOTE,
+                    // the group's slot belongs to its TMEM buffer: free when the
+                    // promotion warps have handed that buffer back
+                    const uint32_t buf = it % NBUF;
+                    if (!ptx::mbar_wait(&tempty[buf], ((it / NBUF) & 1u) ^ 1u, abort_flag, args.err, ERRBIT_PROMOTE,
                                         WAIT_TIMEOUT_NS)) {
                         ok = false;
                         break;
                     }
                     const float *src = raw + rs * L::RAW_FLOATS;
                     const float4 a = *reinterpret_cast<const float4 *>(src + r);
-                    float *dst = scl + ss * L::SCALE_FLOATS;
+                    float *dst = scl + buf * L::SCALE_FLOATS;
 #pragma unroll
                     for (int b = 0; b < L::NBLK; ++b) {
                         const float sb = src[BM + b];
                         *reinterpret_cast<float4 *>(dst + b * BM + r) =
                             make_float4(a.x * sb, a.y * sb, a.z * sb, a.w * sb);
                     }
-                    ptx::mbar_arrive(&sfull[ss]);    // every lane, after its own stores
-                    if (++ss == SCALE_STAGES) {
-                        ss = 0;
-                        sphase ^= 1u;
-                    }
+                    ptx::mbar_arrive(&tfull[buf]);   // every lane, after its own stores
                     if (++rs == L::RAW_SLOTS)
                         rs = 0;
                 }
@@ -484,20 +488,22 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         } else if (warp == SCALE_WARP && !SB_PER_COLUMN) {
             // -------------------------------------------------- scale loader
             // Narrow block-scale tiles: the group's 128 row scales and the
-            // tile's block scale, by cp.async, straight into the slot.
-            int ss = 0;
-            uint32_t sphase = 0;
+            // tile's block scale, by cp.async, straight into the slot of the
+            // group's TMEM buffer; their completion is counted on that buffer's
+            // TMEM-full barrier.
+            uint32_t it = 0;   // global group counter -> TMEM buffer and phase, as the MMA issuers
             bool ok = true;
             for (int tile = work_first; ok && tile < num_work; tile += work_stride) {
                 int tm, tn;
                 coords(tile, tm, tn);
-                for (int g = 0; g < G; ++g) {
-                    if (!ptx::mbar_wait(&sempty[ss], sphase ^ 1u, abort_flag, args.err, ERRBIT_PROMOTE,
+                for (int g = 0; g < G; ++g, ++it) {
+                    const uint32_t buf = it % NBUF;
+                    if (!ptx::mbar_wait(&tempty[buf], ((it / NBUF) & 1u) ^ 1u, abort_flag, args.err, ERRBIT_PROMOTE,
                                         WAIT_TIMEOUT_NS)) {
                         ok = false;
                         break;
                     }
-                    float *dst = scl + ss * L::SCALE_FLOATS;
+                    float *dst = scl + buf * L::SCALE_FLOATS;
                     const float *sa_g = args.sa + static_cast<int64_t>(g) * args.rows;
                     // lane l: rows 4l .. 4l+3 of the tile, one 16-byte copy when
                     // the row count keeps them 16-byte aligned (every row count
@@ -524,11 +530,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                         ptx::cp_async_4(dst + BM, in ? sb_g + static_cast<int64_t>(col >> 7) * args.sb_stride_c : args.sb,
                                         in ? 4u : 0u);
                     }
-                    ptx::cp_async_mbar_arrive_noinc(&sfull[ss]);
-                    if (++ss == SCALE_STAGES) {
-                        ss = 0;
-                        sphase ^= 1u;
-                    }
+                    ptx::cp_async_mbar_arrive_noinc(&tfull[buf]);
                 }
             }
             ptx::cp_async_wait_all();
@@ -567,26 +569,26 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
             for (int g = 0; g < G; ++g, ++it) {
                 const uint32_t buf = it % NBUF;
                 const uint32_t bphase = (it / NBUF) & 1u;
-                if (!ptx::mbar_wait(&sfull[ss], sphase, abort_flag, args.err, ERRBIT_PROMOTE, WAIT_TIMEOUT_NS)) {
+                // Block scales: the TMEM-full barrier also means that the scale
+                // slot of this buffer is written (one wait per group instead of
+                // two: +8 % on the 256-wide Fprop and Dgrad tiles); the slot is
+                // free again with the buffer.  Per-column scales keep their ring.
+                if (SB_PER_COLUMN &&
+                    !ptx::mbar_wait(&sfull[ss], sphase, abort_flag, args.err, ERRBIT_PROMOTE, WAIT_TIMEOUT_NS)) {
                     ok = false;
                     break;
                 }
-                const float *scur = scl + ss * L::SCALE_FLOATS;
+                const float *scur = scl + (SB_PER_COLUMN ? static_cast<uint32_t>(ss) : buf) * L::SCALE_FLOATS;
                 const float *sbcol = scur + BM + wg * COLS_PER_WG;
-                float w_blk = 0.0f;
-                if (!SB_PER_COLUMN) {
-                    if constexpr (L::READY)
-                        w_blk = scur[((wg * COLS_PER_WG) / 128) * BM + row_in_tile];   // the loader's sa * sb
-                    else
-                        w_blk = scur[row_in_tile] * scur[BM];
-                    __syncwarp();
-                    ptx::mbar_arrive_elected(&sempty[ss]);
-                }
-
                 if (!ptx::mbar_wait(&tfull[buf], bphase, abort_flag, args.err, ERRBIT_PROMOTE, WAIT_TIMEOUT_NS)) {
                     ok = false;
                     break;
                 }
+                float w_blk = 0.0f;
+                if constexpr (L::READY)
+                    w_blk = scur[((wg * COLS_PER_WG) / 128) * BM + row_in_tile];   // the loader's sa * sb
+                else if constexpr (!SB_PER_COLUMN)
+                    w_blk = scur[row_in_tile] * scur[BM];
                 ptx::tc_fence_after();
                 if (warp == FIRST_PROMO_WARP) {                  // the group's MMAs are done with it
                     if (SB_PER_COLUMN) {

@@ -264,14 +264,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                 ptx::mbar_init(&empty[s], 1);   // the first promotion warp
             }
             for (int s = 0; s < SCALE_STAGES; ++s) {
-                // per-column scales: the producer's expect-tx arrival; otherwise
-                // every loader lane's copies
-                ptx::mbar_init(&sfull[s], SB_PER_COLUMN ? 1 : 32);
+                // (the scale slots' fill is counted on the TMEM-full barriers)
+                ptx::mbar_init(&sfull[s], 1);
                 ptx::mbar_init(&sempty[s], 4 * NWG);   // one arrival per promotion warp
             }
             for (uint32_t b = 0; b < NBUF; ++b) {
-                // the group's commit; with block scales also every scale-loader lane
-                ptx::mbar_init(&tfull[b], SB_PER_COLUMN ? 1 : 33);
+                // the group's commit, and the scale loader: its expect-tx arrival
+                // (per-column scales) or every one of its lanes (block scales)
+                ptx::mbar_init(&tfull[b], SB_PER_COLUMN ? 2 : 33);
                 ptx::mbar_init(&tempty[b], 4 * NWG);   // one arrival per promotion warp
             }
             ptx::mbar_init(mma_done, 2);   // one final commit per MMA issuer
@@ -305,35 +305,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                 uint32_t issued_mask = 0, issued_parity = 0;
                 const uint64_t pol_a = args.stream_a ? ptx::l2_policy_evict_first() : ptx::l2_policy_evict_normal();
                 const uint64_t pol_b = args.stream_b ? ptx::l2_policy_evict_first() : ptx::l2_policy_evict_normal();
-                int ss = 0;
-                uint32_t sphase = 0;
-                bool scale_pending = false;      // a scale copy this thread started may be in flight
                 bool ok = true;
                 for (int tile = work_first; ok && tile < num_work; tile += work_stride) {
                     int tm, tn;
                     coords(tile, tm, tn);
                     for (int g = 0; g < G; ++g) {
-                        if (SB_PER_COLUMN) {
-                            // the group's 128 row scales and the tile's column scales,
-                            // both contiguous: two bulk copies into the next scale slot
-                            if (!ptx::mbar_wait(&sempty[ss], sphase ^ 1u, abort_flag, args.err, ERRBIT_PRODUCER,
-                                                WAIT_TIMEOUT_NS)) {
-                                ok = false;
-                                break;
-                            }
-                            const int ncol = min(BN, args.cols - tn * BN);
-                            float *dst = scl + ss * L::SCALE_FLOATS;
-                            ptx::mbar_arrive_expect_tx(&sfull[ss], (BM + ncol) * 4);
-                            ptx::bulk_load_1d(dst, args.sa + static_cast<int64_t>(g) * args.rows + tm * BM, BM * 4,
-                                              &sfull[ss]);
-                            ptx::bulk_load_1d(dst + BM, args.sb + static_cast<int64_t>(g) * args.sb_stride_g + tn * BN,
-                                              ncol * 4, &sfull[ss]);
-                            scale_pending = true;
-                            if (++ss == SCALE_STAGES) {
-                                ss = 0;
-                                sphase ^= 1u;
-                            }
-                        }
                         if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, args.err, ERRBIT_PRODUCER,
                                             WAIT_TIMEOUT_NS)) {
                             ok = false;
@@ -356,14 +332,6 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                         if (issued_mask & (1u << s))
                             ptx::mbar_wait(&full[s], (issued_parity >> s) & 1u, nullptr, args.err, ERRBIT_DRAIN,
                                            WAIT_TIMEOUT_NS);
-                    // the scale slots: the most recently filled phase of every slot
-                    if (SB_PER_COLUMN && scale_pending) {
-                        for (int k = 0; k < SCALE_STAGES; ++k) {
-                            const int slot = (ss + SCALE_STAGES - 1 - k) % SCALE_STAGES;
-                            const uint32_t par = slot < ss ? sphase : (sphase ^ 1u);
-                            ptx::mbar_wait(&sfull[slot], par, nullptr, args.err, ERRBIT_DRAIN, WAIT_TIMEOUT_NS);
-                        }
-                    }
                 }
             }
             __syncwarp();
@@ -403,6 +371,58 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                 // all MMAs issued by this thread complete before teardown
                 ptx::mma_commit(mma_done);
                 ptx::mbar_wait(mma_done, 0, nullptr, args.err, ERRBIT_DRAIN, WAIT_TIMEOUT_NS);
+            }
+            __syncwarp();
+        } else if (warp == SCALE_WARP && SB_PER_COLUMN) {
+            // -------------------------------------------------- scale loader
+            // Per-column scales: the group's 128 row scales and the tile's
+            // column scales, both contiguous, by two bulk copies into the next
+            // slot of a 4-slot ring, completing on the TMEM-full barrier of the
+            // group's buffer (which therefore waits for the MMAs and the scales
+            // together).  A slot is free once every promotion warp has handed
+            // back the group that last used it; the copies may only be counted
+            // on the buffer's barrier once its previous group has completed
+            // there.
+            if (lane == 0) {
+                int ss = 0;
+                uint32_t sphase = 0;
+                uint32_t it = 0;   // global group counter -> TMEM buffer and phase
+                bool ok = true;
+                for (int tile = work_first; ok && tile < num_work; tile += work_stride) {
+                    int tm, tn;
+                    coords(tile, tm, tn);
+                    const uint32_t col_bytes = static_cast<uint32_t>(min(BN, args.cols - tn * BN)) * 4u;
+                    const float *sa_g = args.sa + tm * BM;     // group g's row scales, advanced per group
+                    const float *sb_g = args.sb + tn * BN;     // and its column scales
+                    for (int g = 0; g < G; ++g, ++it, sa_g += args.rows, sb_g += args.sb_stride_g) {
+                        const uint32_t buf = it % NBUF;
+                        if (!ptx::mbar_wait(&sempty[ss], sphase ^ 1u, abort_flag, args.err, ERRBIT_PROMOTE,
+                                            WAIT_TIMEOUT_NS) ||
+                            !ptx::mbar_wait(&tfull[buf], ((it / NBUF) & 1u) ^ 1u, abort_flag, args.err,
+                                            ERRBIT_PROMOTE, WAIT_TIMEOUT_NS)) {
+                            ok = false;
+                            break;
+                        }
+                        float *dst = scl + ss * L::SCALE_FLOATS;
+                        ptx::mbar_arrive_expect_tx(&tfull[buf], BM * 4 + col_bytes);
+                        ptx::bulk_load_1d(dst, sa_g, BM * 4, &tfull[buf]);
+                        ptx::bulk_load_1d(dst + BM, sb_g, col_bytes, &tfull[buf]);
+                        if (++ss == SCALE_STAGES) {
+                            ss = 0;
+                            sphase ^= 1u;
+                        }
+                    }
+                }
+                if (!ok) {
+                    // drain: the copies of the last groups must land before exit
+                    // (their barriers complete only with the MMAs' commits too, so
+                    // a wait may also run out: the copies have landed by then)
+                    for (uint32_t k = 0; k < NBUF && k < it; ++k) {
+                        const uint32_t j = it - 1 - k;
+                        ptx::mbar_wait(&tfull[j % NBUF], (j / NBUF) & 1u, nullptr, args.err, ERRBIT_DRAIN,
+                                       WAIT_TIMEOUT_NS);
+                    }
+                }
             }
             __syncwarp();
         } else if (warp == SCALE_WARP && L::READY) {
@@ -569,15 +589,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
             for (int g = 0; g < G; ++g, ++it) {
                 const uint32_t buf = it % NBUF;
                 const uint32_t bphase = (it / NBUF) & 1u;
-                // Block scales: the TMEM-full barrier also means that the scale
-                // slot of this buffer is written (one wait per group instead of
-                // two: +8 % on the 256-wide Fprop and Dgrad tiles); the slot is
-                // free again with the buffer.  Per-column scales keep their ring.
-                if (SB_PER_COLUMN &&
-                    !ptx::mbar_wait(&sfull[ss], sphase, abort_flag, args.err, ERRBIT_PROMOTE, WAIT_TIMEOUT_NS)) {
-                    ok = false;
-                    break;
-                }
+                // The TMEM-full barrier also means that the group's scales have
+                // landed (one wait per group instead of two: +8 % on the 256-wide
+                // Fprop and Dgrad tiles).  Block scales sit in the slot of the
+                // buffer, free again with it; per-column scales, read until the
+                // last multiply-add, in a ring of their own, handed back at the
+                // end of the group.
                 const float *scur = scl + (SB_PER_COLUMN ? static_cast<uint32_t>(ss) : buf) * L::SCALE_FLOATS;
                 const float *sbcol = scur + BM + wg * COLS_PER_WG;
                 if (!ptx::mbar_wait(&tfull[buf], bphase, abort_flag, args.err, ERRBIT_PROMOTE, WAIT_TIMEOUT_NS)) {

@@ -72,20 +72,20 @@ FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1
 # SHA-256 is recorded here (the kernel and its inline-PTX helpers) and is
 # reported as null once they differ.
 GEMM_TRAFFIC = {"per_launch_bytes": {
-                                     "dgrad:down": 640071424,
-                                     "dgrad:gate_up": 2347593472,
-                                     "dgrad:o": 173084672,
-                                     "dgrad:qkv": 222231808,
-                                     "fprop:down": 694206208,
-                                     "fprop:gate_up": 1338408192,
-                                     "fprop:o": 174794496,
-                                     "fprop:qkv": 254276096,
-                                     "wgrad:down": 937095936,
-                                     "wgrad:gate_up": 2341203968,
-                                     "wgrad:o": 306068224,
-                                     "wgrad:qkv": 482590976},
+                                     "dgrad:down": 659678464,
+                                     "dgrad:gate_up": 2359247360,
+                                     "dgrad:o": 173748224,
+                                     "dgrad:qkv": 223385600,
+                                     "fprop:down": 707352832,
+                                     "fprop:gate_up": 1386628608,
+                                     "fprop:o": 175358976,
+                                     "fprop:qkv": 255777280,
+                                     "wgrad:down": 942385408,
+                                     "wgrad:gate_up": 2374707712,
+                                     "wgrad:o": 312825088,
+                                     "wgrad:qkv": 488692224},
                 "sources": ("gemm.cu", "ptx.cuh"),
-                "sha256": "366b4beb3fb4e84e86bfa6199d8bee3a62dd56f376c738046050380ab20f9d4e"}
+                "sha256": "599a2e2bbe613058eeacb5626afa6caf61ea59c8ebe503aa2c2e5a7310dcee26"}
 
 
 def gemm_sources_sha256() -> str:

@@ -230,6 +230,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     constexpr int SECOND_MMA_WARP = 3;
     constexpr uint32_t TMEM_COLS = NBUF * BN;
     static_assert(TMEM_COLS <= 512, "TMEM holds 512 columns");
+    static_assert(TMEM_COLS >= 32 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "an allocation is a power of two >= 32 columns");
     constexpr uint32_t IDESC = ptx::idesc_e4m3_f32(BM, BN);
 
     extern __shared__ uint8_t smem_raw[];

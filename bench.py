@@ -85,7 +85,7 @@ GEMM_TRAFFIC = {"per_launch_bytes": {
                                      "wgrad:o": 312825088,
                                      "wgrad:qkv": 488692224},
                 "sources": ("gemm.cu", "ptx.cuh"),
-                "sha256": "599a2e2bbe613058eeacb5626afa6caf61ea59c8ebe503aa2c2e5a7310dcee26"}
+                "sha256": "1a55eb780703c04f30e08c884a4bbc07cd42d507c627d4cf26ba234ceb425c71"}
 
 
 def gemm_sources_sha256() -> str:

@@ -72,20 +72,20 @@ FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1
 # SHA-256 is recorded here (the kernel and its inline-PTX helpers) and is
 # reported as null once they differ.
 GEMM_TRAFFIC = {"per_launch_bytes": {
-                                     "dgrad:down": 659678464,
-                                     "dgrad:gate_up": 2359247360,
-                                     "dgrad:o": 173748224,
-                                     "dgrad:qkv": 223385600,
-                                     "fprop:down": 707352832,
-                                     "fprop:gate_up": 1386628608,
-                                     "fprop:o": 175358976,
-                                     "fprop:qkv": 255777280,
-                                     "wgrad:down": 942385408,
-                                     "wgrad:gate_up": 2374707712,
-                                     "wgrad:o": 312825088,
-                                     "wgrad:qkv": 488692224},
+                                     "dgrad:down": 641143040,
+                                     "dgrad:gate_up": 2345217280,
+                                     "dgrad:o": 173094656,
+                                     "dgrad:qkv": 222758912,
+                                     "fprop:down": 687700224,
+                                     "fprop:gate_up": 1348172288,
+                                     "fprop:o": 174887168,
+                                     "fprop:qkv": 254118400,
+                                     "wgrad:down": 931030272,
+                                     "wgrad:gate_up": 2336935936,
+                                     "wgrad:o": 306336768,
+                                     "wgrad:qkv": 483261184},
                 "sources": ("gemm.cu", "ptx.cuh"),
-                "sha256": "1a55eb780703c04f30e08c884a4bbc07cd42d507c627d4cf26ba234ceb425c71"}
+                "sha256": "6ed73b2241557cc4a015dbd8cceebe982df2567975910b738c53256055d3847f"}
 
 
 def gemm_sources_sha256() -> str:

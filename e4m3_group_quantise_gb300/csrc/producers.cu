@@ -31,18 +31,22 @@ constexpr int PR_THREADS = 256;
 constexpr int PR_WARPS = PR_THREADS / 32;
 
 // Hardware approximations of 2^x and 1/x (deterministic; the relative
-// error of each is a few fp32 ulps, subnormal results kept).
+// error of each is a few fp32 ulps), in their flush-to-zero forms, which need
+// no extra instructions around the hardware unit.  In the sigmoid
+// 1 / (1 + 2^a) that changes no result: a subnormal a gives 2^a = 1 either
+// way, a subnormal 2^a vanishes next to the 1 it is added to, and the
+// reciprocal's argument is at least 1.
 __device__ __forceinline__ float ex2_approx(float x)
 {
     float r;
-    asm("ex2.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
     return r;
 }
 
 __device__ __forceinline__ float rcp_approx(float x)
 {
     float r;
-    asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
     return r;
 }
 

@@ -33,9 +33,11 @@ constexpr int PR_WARPS = PR_THREADS / 32;
 // Hardware approximations of 2^x and 1/x (deterministic; the relative
 // error of each is a few fp32 ulps), in their flush-to-zero forms, which need
 // no extra instructions around the hardware unit.  In the sigmoid
-// 1 / (1 + 2^a) that changes no result: a subnormal a gives 2^a = 1 either
-// way, a subnormal 2^a vanishes next to the 1 it is added to, and the
-// reciprocal's argument is at least 1.
+// 1 / (1 + 2^a) that changes nothing above gates of about -87.3: a subnormal
+// a gives 2^a = 1 either way, a subnormal 2^a vanishes next to the 1 it is
+// added to, and the reciprocal's argument is at least 1.  Below, the
+// sigmoid itself would be subnormal and is 0 instead -- within the bound
+// stated for gates below -87.
 __device__ __forceinline__ float ex2_approx(float x)
 {
     float r;

@@ -13,10 +13,11 @@
 // value (nearest even) is then quantised exactly as jetfp8_quantize_act
 // quantises it, and the optional bf16 output is that same value.
 //
-// Layout of the work: a lane holds eight consecutive values (one 16-byte
-// vector) of a 256-column chunk, so a 1x128 group is one half-warp: its
-// amax takes four shuffles and its codes leave as one contiguous 128-byte
-// store.
+// Layout of the work: a lane holds 32 consecutive values (four 16-byte
+// vectors, a "quad"), so a 1x128 group is four neighbouring lanes: its amax
+// takes two shuffles, its scale is computed once per 32 values, and each
+// lane's codes leave as 32 contiguous bytes.  (Rows wider than 32768
+// columns fall back to eight values per lane, a group per half-warp.)
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <cstdint>
@@ -65,20 +66,30 @@ __device__ __forceinline__ void round_bf16x8(const float (&v)[8], uint32_t (&w)[
     }
 }
 
+// The same for 32 values (four 16-byte vectors' worth).
+__device__ __forceinline__ void round_bf16x32(const float (&v)[32], uint32_t (&w)[16], float (&r)[32])
+{
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * k], v[2 * k + 1]);
+        w[k] = *reinterpret_cast<const uint32_t *>(&h);
+        r[2 * k] = bf16_lo(w[k]);
+        r[2 * k + 1] = bf16_hi(w[k]);
+    }
+}
+
 // ---------------------------------------------------------------------------
 // RMSNorm.  The sum of squares of a row: each thread adds, in order, the
-// squares of its chunks' values (with four warps per row: even and odd
-// values in two chains, added at the end); the lanes of a warp combine by butterfly
-// (partner distance 16, 8, 4, 2, 1); the warps of the row then add up in
-// warp order.  y = bf16((x * rstd) * gamma) is then quantised per 1x128
-// group.  Rows of up to RN_REG_MAX_H columns: four warps per row (two rows
-// per block), each thread's 16-byte chunks t, t + 128, ... held in registers
-// between the two steps, so the row is read from memory once.  Wider rows:
-// one warp per row, the row read a second time (from cache).
+// squares of its values (even and odd values in two chains, added at the
+// end; with one warp per row, a single chain); the lanes of a warp combine by
+// butterfly (partner distance 16, 8, 4, 2, 1); the warps of the row then add
+// up in warp order.  y = bf16((x * rstd) * gamma) is then quantised per 1x128
+// group.  Rows of up to RN_REG_MAX_H columns: up to eight warps per row,
+// each thread's quads held in registers between the two steps, so the row is
+// read from memory once.  Wider rows: one warp per row, the row read a
+// second time (from cache).
 // ---------------------------------------------------------------------------
-constexpr int RN_ROW_THREADS = 128;
-constexpr int RN_ROWS = PR_THREADS / RN_ROW_THREADS;
-constexpr int64_t RN_REG_MAX_H = 16384;      // 16 chunks of 8 values per thread
+constexpr int64_t RN_REG_MAX_H = 32768;      // eight warps of four quads (32 values each) per row
 
 __device__ __forceinline__ float sum_squares8(float acc, const uint4 &c)
 {
@@ -143,54 +154,105 @@ __device__ __forceinline__ void rms_chunk_out(const uint4 &xc, const uint4 &gc, 
         quantize8_halfwarp(v, w, q + row * H + 8 * c, s + (c >> 4) * M + row, lane);
 }
 
-// (rows of up to 4096 columns: capped for five blocks per SM, +3 % measured)
-template <int JMAX>
-__global__ void __launch_bounds__(PR_THREADS, JMAX <= 4 ? 5 : 1)
-rmsnorm_quantize_kernel(const uint4 *__restrict__ x, const uint4 *__restrict__ gamma, float eps, int64_t M,
-                        int64_t H, uint8_t *__restrict__ q, float *__restrict__ s, uint4 *__restrict__ y)
+// y = bf16((x * rstd) * gamma) of one quad (32 consecutive values, four
+// 16-byte vectors xq) of a row, starting at column 32 qd: stored to y and / or
+// quantised (the four lanes 4k .. 4k+3 of a warp hold one 1x128 group).  Every
+// lane of the warp takes part; a lane whose quad is past the row's end
+// (`live` false) stores nothing.
+__device__ __forceinline__ void rms_quad_out(const uint4 (&xq)[4], const uint4 (&gq)[4], bool live,
+                                             float rstd, int64_t row, int64_t qd, int64_t M, int64_t H,
+                                             uint8_t *__restrict__ q, float *__restrict__ s,
+                                             uint4 *__restrict__ y, int lane)
 {
-    __shared__ float part[RN_ROWS][RN_ROW_THREADS / 32];
-    const int lane = threadIdx.x & 31;
-    const int t = threadIdx.x % RN_ROW_THREADS;
-    const int r_in_block = threadIdx.x / RN_ROW_THREADS;
-    const int64_t row = static_cast<int64_t>(blockIdx.x) * RN_ROWS + r_in_block;
-    const bool live = row < M;                    // no early exit: the block meets at a barrier
-    const int64_t H8 = H >> 3;
-    const uint4 *xr = x + (live ? row : 0) * H8;
-
-    // chunks t + 128 j below H8; H8 is a multiple of 32, so a warp's lanes
-    // are all in or all out
-    uint4 v[JMAX];
+    const uint64_t r2 = ptx::pack_f32x2(rstd, rstd);
+    float u[32];
 #pragma unroll
-    for (int j = 0; j < JMAX; ++j)
-        if (live && t + RN_ROW_THREADS * j < H8)
-            v[j] = __ldg(xr + t + RN_ROW_THREADS * j);
+    for (int k = 0; k < 4; ++k) {
+        float f[8], g[8];
+        unpack8(xq[k], f);
+        unpack8(gq[k], g);
+        // (x * rstd) * gamma, two values per packed multiply (each lane
+        // rounded as the scalar multiply)
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+            const uint64_t xr2 = ptx::mul_f32x2(ptx::pack_f32x2(f[e], f[e + 1]), r2);
+            const uint64_t y2 = ptx::mul_f32x2(xr2, ptx::pack_f32x2(g[e], g[e + 1]));
+            u[8 * k + e] = ptx::lo_f32(y2);
+            u[8 * k + e + 1] = ptx::hi_f32(y2);
+        }
+    }
+    uint32_t w[16];
+    float v[32];
+    round_bf16x32(u, w, v);
+    if (y && live) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            y[row * (H >> 3) + 4 * qd + k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+    }
+    if (q)
+        quantize32_quad(v, w, live, q + row * H + 32 * qd, s + (qd >> 2) * M + row, lane);
+}
+
+// A row is taken by `rw` warps (rw 32 threads: thread t holds quads t,
+// t + 32 rw, ...), 8 / rw rows per block (one when rw > 4); each thread holds
+// at most JQ quads, so the row is read from memory once.
+template <int JQ>
+__global__ void __launch_bounds__(PR_THREADS)
+rmsnorm_quantize_kernel(const uint4 *__restrict__ x, const uint4 *__restrict__ gamma, float eps, int64_t M,
+                        int64_t H, int rw, uint8_t *__restrict__ q, float *__restrict__ s, uint4 *__restrict__ y)
+{
+    __shared__ float part[PR_WARPS];
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int row_threads = 32 * rw;
+    const int t = threadIdx.x % row_threads;
+    const int r_in_block = threadIdx.x / row_threads;
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x / row_threads) + r_in_block;
+    const bool live = row < M;                    // no early exit: the block meets at a barrier
+    const int64_t NQ = H >> 5;                    // quads per row (a multiple of 4: groups are whole)
+    const uint4 *xr = x + (live ? row : 0) * (H >> 3);
+
+    uint4 v[JQ][4];
+#pragma unroll
+    for (int j = 0; j < JQ; ++j) {
+        const int64_t qd = t + static_cast<int64_t>(row_threads) * j;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            v[j][k] = live && qd < NQ ? __ldg(xr + 4 * qd + k) : make_uint4(0u, 0u, 0u, 0u);
+    }
     // squares summed as two interleaved fp32 chains (even and odd values,
-    // one packed fused multiply-add per pair), then added
+    // one packed fused multiply-add per pair; zero-filled quads add +0),
+    // then added
     uint64_t acc2 = 0ull;
 #pragma unroll
-    for (int j = 0; j < JMAX; ++j)
-        if (live && t + RN_ROW_THREADS * j < H8)
-            acc2 = sum_squares8x2(acc2, v[j]);
+    for (int j = 0; j < JQ; ++j)
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            acc2 = sum_squares8x2(acc2, v[j][k]);
     float acc = __fadd_rn(ptx::lo_f32(acc2), ptx::hi_f32(acc2));
 #pragma unroll
     for (int d = 16; d >= 1; d >>= 1)
         acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, d));
     if (lane == 0)
-        part[r_in_block][t >> 5] = acc;
+        part[warp] = acc;
     __syncthreads();
-    float sum_sq = part[r_in_block][0];
-#pragma unroll
-    for (int w = 1; w < RN_ROW_THREADS / 32; ++w)
-        sum_sq = __fadd_rn(sum_sq, part[r_in_block][w]);
+    const int w0 = r_in_block * rw;               // the row's first warp
+    float sum_sq = part[w0];
+    for (int w = 1; w < rw; ++w)
+        sum_sq = __fadd_rn(sum_sq, part[w0 + w]);
     if (!live)
-        return;
+        return;                                   // whole rows, so whole groups
     const float rstd = rms_rstd(sum_sq, H, eps);
 #pragma unroll
-    for (int j = 0; j < JMAX; ++j) {
-        const int64_t c = t + RN_ROW_THREADS * j;
-        if (c < H8)
-            rms_chunk_out(v[j], __ldg(gamma + c), rstd, row, c, M, H, q, s, y, lane);
+    for (int j = 0; j < JQ; ++j) {
+        const int64_t qd = t + static_cast<int64_t>(row_threads) * j;
+        if ((t & ~31) + static_cast<int64_t>(row_threads) * j < NQ) {   // some lane of the warp is in the row
+            uint4 g[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                g[k] = qd < NQ ? __ldg(gamma + 4 * qd + k) : make_uint4(0u, 0u, 0u, 0u);
+            rms_quad_out(v[j], g, qd < NQ, rstd, row, qd, M, H, q, s, y, lane);
+        }
     }
 }
 
@@ -222,8 +284,9 @@ rmsnorm_quantize_wide_kernel(const uint4 *__restrict__ x, const uint4 *__restric
 
 // ---------------------------------------------------------------------------
 // SwiGLU of a gate_up output [M][2I] (gate = columns 0..I-1, up = I..2I-1):
-// y = bf16( (g * (1 / (1 + e^-g))) * u ).  A warp handles one 256-column
-// chunk of one row per iteration (grid-stride over all chunks).
+// y = bf16( (g * (1 / (1 + e^-g))) * u ).  A warp handles four 256-column
+// chunks per iteration, eight lanes (one quad each) per chunk, grid-stride
+// over all chunks.
 //
 // Accuracy: -g log2 e is rounded once, which moves the exponent by at most
 // 2^-24 |g log2 e| <= 2^-17 where 2^(-g log2 e) is finite and normal, i.e. a
@@ -240,35 +303,51 @@ __global__ void __launch_bounds__(PR_THREADS)
 swiglu_quantize_kernel(const uint4 *__restrict__ gu, int64_t M, int64_t I, uint8_t *__restrict__ q,
                        float *__restrict__ s, uint4 *__restrict__ y)
 {
+    // A warp takes four 256-column chunks (items) per iteration, eight lanes
+    // per chunk, each lane four consecutive 16-byte vectors (32 outputs): a
+    // 1x128 group is four lanes.
     const int lane = threadIdx.x & 31;
-    const int64_t chunks = I >> 8;
+    const int sub = lane & 7;                     // lane within its chunk's eight
+    const int64_t chunks = I >> 8;                // 256-column chunks per row
     const int64_t items = M * chunks;
     const int64_t in_row = I >> 2;                // uint4 per gate_up row (2I bf16)
     const int64_t out_row = I >> 3;               // uint4 per output row
-    for (int64_t it = static_cast<int64_t>(blockIdx.x) * PR_WARPS + (threadIdx.x >> 5); it < items;
-         it += static_cast<int64_t>(gridDim.x) * PR_WARPS) {
-        const int64_t row = it / chunks;
-        const int64_t c = (it - row * chunks) * 32 + lane;   // output uint4 index within the row
-        float g[8], u[8], t[8], v[8];
-        unpack8(__ldg(gu + row * in_row + c), g);
-        unpack8(__ldg(gu + row * in_row + out_row + c), u);
+    const int64_t step = static_cast<int64_t>(gridDim.x) * PR_WARPS * 4;
+    for (int64_t base = (static_cast<int64_t>(blockIdx.x) * PR_WARPS + (threadIdx.x >> 5)) * 4; base < items;
+         base += step) {
+        const int64_t it = base + (lane >> 3);
+        const bool live = it < items;             // (a lane past the end still joins the group's shuffles)
+        const int64_t row = live ? it / chunks : 0;
+        const int64_t c0 = (live ? it - row * chunks : 0) * 32 + 4 * sub;   // first output uint4 of the lane
+        float t[32];
 #pragma unroll
-        for (int e = 0; e < 8; e += 2) {
-            // sigmoid(g) = 1 / (1 + 2^(-g log2 e))
-            const uint64_t a = ptx::mul_f32x2(ptx::pack_f32x2(g[e], g[e + 1]), ptx::pack_f32x2(-LOG2E, -LOG2E));
-            const float s0 = rcp_approx(__fadd_rn(1.0f, ex2_approx(ptx::lo_f32(a))));
-            const float s1 = rcp_approx(__fadd_rn(1.0f, ex2_approx(ptx::hi_f32(a))));
-            const uint64_t gs = ptx::mul_f32x2(ptx::pack_f32x2(g[e], g[e + 1]), ptx::pack_f32x2(s0, s1));
-            const uint64_t tu = ptx::mul_f32x2(gs, ptx::pack_f32x2(u[e], u[e + 1]));
-            t[e] = ptx::lo_f32(tu);
-            t[e + 1] = ptx::hi_f32(tu);
+        for (int j = 0; j < 4; ++j) {
+            float g[8], u[8];
+            unpack8(__ldg(gu + row * in_row + c0 + j), g);
+            unpack8(__ldg(gu + row * in_row + out_row + c0 + j), u);
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) {
+                // sigmoid(g) = 1 / (1 + 2^(-g log2 e))
+                const uint64_t a =
+                    ptx::mul_f32x2(ptx::pack_f32x2(g[e], g[e + 1]), ptx::pack_f32x2(-LOG2E, -LOG2E));
+                const float s0 = rcp_approx(__fadd_rn(1.0f, ex2_approx(ptx::lo_f32(a))));
+                const float s1 = rcp_approx(__fadd_rn(1.0f, ex2_approx(ptx::hi_f32(a))));
+                const uint64_t gs = ptx::mul_f32x2(ptx::pack_f32x2(g[e], g[e + 1]), ptx::pack_f32x2(s0, s1));
+                const uint64_t tu = ptx::mul_f32x2(gs, ptx::pack_f32x2(u[e], u[e + 1]));
+                t[8 * j + e] = ptx::lo_f32(tu);
+                t[8 * j + e + 1] = ptx::hi_f32(tu);
+            }
         }
-        uint32_t w[4];
-        round_bf16x8(t, w, v);
-        if (y)
-            y[row * out_row + c] = make_uint4(w[0], w[1], w[2], w[3]);
+        uint32_t w[16];
+        float v[32];
+        round_bf16x32(t, w, v);
+        if (y && live) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                y[row * out_row + c0 + j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+        }
         if (q)
-            quantize8_halfwarp(v, w, q + row * I + 8 * c, s + (c >> 4) * M + row, lane);
+            quantize32_quad(v, w, live, q + row * I + 8 * c0, s + (c0 >> 4) * M + row, lane);
     }
 }
 
@@ -286,16 +365,19 @@ cudaError_t launch_rmsnorm_quantize(const void *x, const void *gamma, float eps,
                                                                                                s, yv);
         return cudaGetLastError();
     }
-    const unsigned blocks = static_cast<unsigned>((M + RN_ROWS - 1) / RN_ROWS);
-    // chunks of 8 values per thread: H / 8 / 128, rounded up
-    if (H <= 4096)
-        rmsnorm_quantize_kernel<4><<<blocks, PR_THREADS, 0, stream>>>(xv, gv, eps, M, H, q, s, yv);
-    else if (H <= 5120)
-        rmsnorm_quantize_kernel<5><<<blocks, PR_THREADS, 0, stream>>>(xv, gv, eps, M, H, q, s, yv);
-    else if (H <= 8192)
-        rmsnorm_quantize_kernel<8><<<blocks, PR_THREADS, 0, stream>>>(xv, gv, eps, M, H, q, s, yv);
+    // the fewest quads per thread (1, 2 or 4) that keep a row within eight warps
+    const int64_t NQ = H >> 5;
+    const int jq = NQ <= 256 ? 1 : NQ <= 512 ? 2 : 4;
+    const int rw = static_cast<int>((NQ + 32 * jq - 1) / (32 * jq));
+    const int rows = rw <= 4 ? PR_WARPS / rw : 1;
+    const unsigned blocks = static_cast<unsigned>((M + rows - 1) / rows);
+    const unsigned threads = static_cast<unsigned>(rows * rw * 32);
+    if (jq == 1)
+        rmsnorm_quantize_kernel<1><<<blocks, threads, 0, stream>>>(xv, gv, eps, M, H, rw, q, s, yv);
+    else if (jq == 2)
+        rmsnorm_quantize_kernel<2><<<blocks, threads, 0, stream>>>(xv, gv, eps, M, H, rw, q, s, yv);
     else
-        rmsnorm_quantize_kernel<16><<<blocks, PR_THREADS, 0, stream>>>(xv, gv, eps, M, H, q, s, yv);
+        rmsnorm_quantize_kernel<4><<<blocks, threads, 0, stream>>>(xv, gv, eps, M, H, rw, q, s, yv);
     return cudaGetLastError();
 }
 
@@ -303,7 +385,7 @@ cudaError_t launch_swiglu_quantize(const void *gu, int64_t M, int64_t I, uint8_t
                                    int sm_count, cudaStream_t stream)
 {
     const int64_t items = M * (I >> 8);
-    const int64_t want = (items + PR_WARPS - 1) / PR_WARPS;
+    const int64_t want = (items + 4 * PR_WARPS - 1) / (4 * PR_WARPS);   // four chunks per warp and iteration
     const int64_t cap = static_cast<int64_t>(sm_count) * 8;    // 8 resident blocks per SM
     const int64_t blocks = want < cap ? want : cap;
     swiglu_quantize_kernel<<<static_cast<unsigned>(blocks), PR_THREADS, 0, stream>>>(

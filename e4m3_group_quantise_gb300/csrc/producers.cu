@@ -84,12 +84,13 @@ __device__ __forceinline__ void round_bf16x32(const float (&v)[32], uint32_t (&w
 // end; with one warp per row, a single chain); the lanes of a warp combine by
 // butterfly (partner distance 16, 8, 4, 2, 1); the warps of the row then add
 // up in warp order.  y = bf16((x * rstd) * gamma) is then quantised per 1x128
-// group.  Rows of up to RN_REG_MAX_H columns: up to eight warps per row,
+// group.  Rows of up to RN_REG_MAX_H columns: up to sixteen warps per row,
 // each thread's quads held in registers between the two steps, so the row is
 // read from memory once.  Wider rows: one warp per row, the row read a
 // second time (from cache).
 // ---------------------------------------------------------------------------
-constexpr int64_t RN_REG_MAX_H = 32768;      // eight warps of four quads (32 values each) per row
+constexpr int RN_MAX_THREADS = 512;           // up to sixteen warps per row
+constexpr int64_t RN_REG_MAX_H = 32768;      // sixteen warps of two quads (32 values each) per row
 
 __device__ __forceinline__ float sum_squares8(float acc, const uint4 &c)
 {
@@ -195,13 +196,15 @@ __device__ __forceinline__ void rms_quad_out(const uint4 (&xq)[4], const uint4 (
 
 // A row is taken by `rw` warps (rw 32 threads: thread t holds quads t,
 // t + 32 rw, ...), 8 / rw rows per block (one when rw > 4); each thread holds
-// at most JQ quads, so the row is read from memory once.
+// at most JQ quads, so the row is read from memory once.  (With one quad per
+// thread, capped at 64 registers: more resident warps hide the loads better
+// than a larger register budget; measured.)
 template <int JQ>
-__global__ void __launch_bounds__(PR_THREADS)
+__global__ void __launch_bounds__(RN_MAX_THREADS, JQ == 1 ? 2 : 1)
 rmsnorm_quantize_kernel(const uint4 *__restrict__ x, const uint4 *__restrict__ gamma, float eps, int64_t M,
                         int64_t H, int rw, uint8_t *__restrict__ q, float *__restrict__ s, uint4 *__restrict__ y)
 {
-    __shared__ float part[PR_WARPS];
+    __shared__ float part[RN_MAX_THREADS / 32];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int row_threads = 32 * rw;
@@ -365,19 +368,19 @@ cudaError_t launch_rmsnorm_quantize(const void *x, const void *gamma, float eps,
                                                                                                s, yv);
         return cudaGetLastError();
     }
-    // the fewest quads per thread (1, 2 or 4) that keep a row within eight warps
+    // one quad per thread up to eight warps per row (8192 columns), else two
+    // (sixteen warps of one quad measured slower at 16384 columns: 3.20
+    // against 3.31 TB/s)
     const int64_t NQ = H >> 5;
-    const int jq = NQ <= 256 ? 1 : NQ <= 512 ? 2 : 4;
+    const int jq = NQ <= 256 ? 1 : 2;
     const int rw = static_cast<int>((NQ + 32 * jq - 1) / (32 * jq));
     const int rows = rw <= 4 ? PR_WARPS / rw : 1;
     const unsigned blocks = static_cast<unsigned>((M + rows - 1) / rows);
     const unsigned threads = static_cast<unsigned>(rows * rw * 32);
     if (jq == 1)
         rmsnorm_quantize_kernel<1><<<blocks, threads, 0, stream>>>(xv, gv, eps, M, H, rw, q, s, yv);
-    else if (jq == 2)
-        rmsnorm_quantize_kernel<2><<<blocks, threads, 0, stream>>>(xv, gv, eps, M, H, rw, q, s, yv);
     else
-        rmsnorm_quantize_kernel<4><<<blocks, threads, 0, stream>>>(xv, gv, eps, M, H, rw, q, s, yv);
+        rmsnorm_quantize_kernel<2><<<blocks, threads, 0, stream>>>(xv, gv, eps, M, H, rw, q, s, yv);
     return cudaGetLastError();
 }
 

@@ -107,6 +107,36 @@ def test_rmsnorm_8b_training_size():
     check_rmsnorm(x, gamma, 1e-6, "rmsnorm 16384x4096")
 
 
+def many_rows():
+    """A row count of several rows per SM plus a ragged remainder."""
+    return 8 * torch.cuda.get_device_properties(0).multi_processor_count + 37
+
+
+@pytest.mark.parametrize("H", [256, 5120, 16384])
+def test_rmsnorm_parity_many_rows(H):
+    """One warp per row (H 256, eight rows per block), five warps of one quad
+    per thread (5120, one row per block), eight warps of two quads (16384)."""
+    M = many_rows()
+    x = syn.activation(M, H, seed=H + 1, outlier_scale=20.0, device=DEV)
+    gamma = (syn.normal_bf16((H,), 0.1, seed=H, tensor="w", device=DEV) + 1.0).to(torch.bfloat16)
+    check_rmsnorm(x, gamma, 1e-6, f"rmsnorm {M}x{H}")
+
+
+@pytest.mark.parametrize("H", [4096, 8192, 16384, 32768])
+def test_rmsnorm_rows_batch_invariant(H):
+    """A row's bits do not depend on the batch: rows of a large batch equal
+    the same rows normalised alone or in small batches (one to sixteen warps
+    per row, one or two quads per thread)."""
+    M = many_rows()
+    x = syn.activation(M, H, seed=H + 2, outlier_scale=20.0, device=DEV)
+    gamma = (syn.normal_bf16((H,), 0.1, seed=H + 3, tensor="w", device=DEV) + 1.0).to(torch.bfloat16)
+    q, s, y = jf.rmsnorm_quantize_act(x, gamma, 1e-6, want_y=True)
+    assert jf.jetfp8_poll_device_error() == 0
+    for a, b in [(0, 1), (5, 69), (M - 40, M)]:
+        qa, sa, ya = jf.rmsnorm_quantize_act(x[a:b].contiguous(), gamma, 1e-6, want_y=True)
+        assert torch.equal(ya, y[a:b]) and torch.equal(qa, q[a:b]) and torch.equal(sa, s[:, a:b])
+
+
 @pytest.mark.parametrize("M,I", [(1, 256), (7, 512), (256, 1536), (300, 14336), (64, 27648)])
 def test_swiglu_parity(M, I):
     gu = syn.activation(M, 2 * I, seed=M + I, outlier_scale=20.0, device=DEV)

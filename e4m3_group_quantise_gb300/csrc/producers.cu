@@ -13,11 +13,14 @@
 // value (nearest even) is then quantised exactly as jetfp8_quantize_act
 // quantises it, and the optional bf16 output is that same value.
 //
-// Layout of the work: a lane holds 32 consecutive values (four 16-byte
-// vectors, a "quad"), so a 1x128 group is four neighbouring lanes: its amax
-// takes two shuffles, its scale is computed once per 32 values, and each
-// lane's codes leave as 32 contiguous bytes.  (Rows wider than 32768
-// columns fall back to eight values per lane, a group per half-warp.)
+// Layout of the work: a 1x128 group (sixteen 16-byte pieces) is held by four
+// neighbouring lanes, lane l of the four holding pieces l, l + 4, l + 8 and
+// l + 12 (its "quad", 32 values): the group's amax takes two shuffles, its
+// scale is computed once per 32 values, and each load or store instruction
+// of a warp touches eight 64-byte runs (eight cache lines) instead of
+// sixteen lines for a lane holding four consecutive pieces -- the cache's
+// request throughput, not DRAM, was the tighter limit.  (Rows wider than
+// 32768 columns fall back to eight values per lane, a group per half-warp.)
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <cstdint>
@@ -155,13 +158,13 @@ __device__ __forceinline__ void rms_chunk_out(const uint4 &xc, const uint4 &gc, 
         quantize8_halfwarp(v, w, q + row * H + 8 * c, s + (c >> 4) * M + row, lane);
 }
 
-// y = bf16((x * rstd) * gamma) of one quad (32 consecutive values, four
-// 16-byte vectors xq) of a row, starting at column 32 qd: stored to y and / or
-// quantised (the four lanes 4k .. 4k+3 of a warp hold one 1x128 group).  Every
-// lane of the warp takes part; a lane whose quad is past the row's end
-// (`live` false) stores nothing.
+// y = bf16((x * rstd) * gamma) of one quad of a row: the pieces p0 + 4k
+// (k = 0..3, xq and gq) of the group p0 >> 4, stored to y and / or quantised
+// (the group's four lanes are neighbours in the warp).  Every lane of the
+// warp takes part; a lane whose quad is past the row's end (`live` false)
+// stores nothing.
 __device__ __forceinline__ void rms_quad_out(const uint4 (&xq)[4], const uint4 (&gq)[4], bool live,
-                                             float rstd, int64_t row, int64_t qd, int64_t M, int64_t H,
+                                             float rstd, int64_t row, int64_t p0, int64_t M, int64_t H,
                                              uint8_t *__restrict__ q, float *__restrict__ s,
                                              uint4 *__restrict__ y, int lane)
 {
@@ -188,10 +191,16 @@ __device__ __forceinline__ void rms_quad_out(const uint4 (&xq)[4], const uint4 (
     if (y && live) {
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-            y[row * (H >> 3) + 4 * qd + k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+            y[row * (H >> 3) + p0 + 4 * k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
     }
     if (q)
-        quantize32_quad(v, w, live, q + row * H + 32 * qd, s + (qd >> 2) * M + row, lane);
+        quantize32_quad<32>(v, w, live, q + row * H + 8 * p0, s + (p0 >> 4) * M + row, lane);
+}
+
+// first piece of quad qd: group qd >> 2, lane qd & 3 of the group's four
+__device__ __forceinline__ int64_t quad_first_piece(int64_t qd)
+{
+    return 16 * (qd >> 2) + (qd & 3);
 }
 
 // A row is taken by `rw` warps (rw 32 threads: thread t holds quads t,
@@ -219,9 +228,10 @@ rmsnorm_quantize_kernel(const uint4 *__restrict__ x, const uint4 *__restrict__ g
 #pragma unroll
     for (int j = 0; j < JQ; ++j) {
         const int64_t qd = t + static_cast<int64_t>(row_threads) * j;
+        const int64_t p0 = quad_first_piece(qd);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-            v[j][k] = live && qd < NQ ? __ldg(xr + 4 * qd + k) : make_uint4(0u, 0u, 0u, 0u);
+            v[j][k] = live && qd < NQ ? __ldg(xr + p0 + 4 * k) : make_uint4(0u, 0u, 0u, 0u);
     }
     // squares summed as two interleaved fp32 chains (even and odd values,
     // one packed fused multiply-add per pair; zero-filled quads add +0),
@@ -250,11 +260,12 @@ rmsnorm_quantize_kernel(const uint4 *__restrict__ x, const uint4 *__restrict__ g
     for (int j = 0; j < JQ; ++j) {
         const int64_t qd = t + static_cast<int64_t>(row_threads) * j;
         if ((t & ~31) + static_cast<int64_t>(row_threads) * j < NQ) {   // some lane of the warp is in the row
+            const int64_t p0 = quad_first_piece(qd);
             uint4 g[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-                g[k] = qd < NQ ? __ldg(gamma + 4 * qd + k) : make_uint4(0u, 0u, 0u, 0u);
-            rms_quad_out(v[j], g, qd < NQ, rstd, row, qd, M, H, q, s, y, lane);
+                g[k] = qd < NQ ? __ldg(gamma + p0 + 4 * k) : make_uint4(0u, 0u, 0u, 0u);
+            rms_quad_out(v[j], g, qd < NQ, rstd, row, p0, M, H, q, s, y, lane);
         }
     }
 }
@@ -307,8 +318,8 @@ swiglu_quantize_kernel(const uint4 *__restrict__ gu, int64_t M, int64_t I, uint8
                        float *__restrict__ s, uint4 *__restrict__ y)
 {
     // A warp takes four 256-column chunks (items) per iteration, eight lanes
-    // per chunk, each lane four consecutive 16-byte vectors (32 outputs): a
-    // 1x128 group is four lanes.
+    // per chunk (its two 1x128 groups), each lane a quad: pieces c0 + 4j of
+    // the output row (32 outputs).
     const int lane = threadIdx.x & 31;
     const int sub = lane & 7;                     // lane within its chunk's eight
     const int64_t chunks = I >> 8;                // 256-column chunks per row
@@ -321,13 +332,13 @@ swiglu_quantize_kernel(const uint4 *__restrict__ gu, int64_t M, int64_t I, uint8
         const int64_t it = base + (lane >> 3);
         const bool live = it < items;             // (a lane past the end still joins the group's shuffles)
         const int64_t row = live ? it / chunks : 0;
-        const int64_t c0 = (live ? it - row * chunks : 0) * 32 + 4 * sub;   // first output uint4 of the lane
+        const int64_t c0 = (live ? it - row * chunks : 0) * 32 + 16 * (sub >> 2) + (sub & 3);   // first piece
         float t[32];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             float g[8], u[8];
-            unpack8(__ldg(gu + row * in_row + c0 + j), g);
-            unpack8(__ldg(gu + row * in_row + out_row + c0 + j), u);
+            unpack8(__ldg(gu + row * in_row + c0 + 4 * j), g);
+            unpack8(__ldg(gu + row * in_row + out_row + c0 + 4 * j), u);
 #pragma unroll
             for (int e = 0; e < 8; e += 2) {
                 // sigmoid(g) = 1 / (1 + 2^(-g log2 e))
@@ -347,10 +358,10 @@ swiglu_quantize_kernel(const uint4 *__restrict__ gu, int64_t M, int64_t I, uint8
         if (y && live) {
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-                y[row * out_row + c0 + j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+                y[row * out_row + c0 + 4 * j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
         }
         if (q)
-            quantize32_quad(v, w, live, q + row * I + 8 * c0, s + (c0 >> 4) * M + row, lane);
+            quantize32_quad<32>(v, w, live, q + row * I + 8 * c0, s + (c0 >> 4) * M + row, lane);
     }
 }
 

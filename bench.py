@@ -72,20 +72,20 @@ FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1
 # SHA-256 is recorded here (the kernel and its inline-PTX helpers) and is
 # reported as null once they differ.
 GEMM_TRAFFIC = {"per_launch_bytes": {
-                                     "dgrad:down": 641143040,
-                                     "dgrad:gate_up": 2345217280,
-                                     "dgrad:o": 173094656,
-                                     "dgrad:qkv": 222758912,
-                                     "fprop:down": 687700224,
-                                     "fprop:gate_up": 1348172288,
-                                     "fprop:o": 174887168,
-                                     "fprop:qkv": 254118400,
-                                     "wgrad:down": 931030272,
-                                     "wgrad:gate_up": 2336935936,
-                                     "wgrad:o": 306336768,
-                                     "wgrad:qkv": 483261184},
+                                     "dgrad:down": 635900416,
+                                     "dgrad:gate_up": 2344995840,
+                                     "dgrad:o": 172978688,
+                                     "dgrad:qkv": 222512128,
+                                     "fprop:down": 666591488,
+                                     "fprop:gate_up": 1331336704,
+                                     "fprop:o": 174819584,
+                                     "fprop:qkv": 254374912,
+                                     "wgrad:down": 934543872,
+                                     "wgrad:gate_up": 2348488192,
+                                     "wgrad:o": 306686208,
+                                     "wgrad:qkv": 483127552},
                 "sources": ("gemm.cu", "ptx.cuh"),
-                "sha256": "6ed73b2241557cc4a015dbd8cceebe982df2567975910b738c53256055d3847f"}
+                "sha256": "810dd5c2a92e557fff4058aeb4747920215b59d1f729c3eeb46f85282b8c0ad3"}
 
 
 def gemm_sources_sha256() -> str:

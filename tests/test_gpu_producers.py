@@ -70,8 +70,11 @@ def check_swiglu(gu, what):
     return q, s, y
 
 
-@pytest.mark.parametrize("M,H", [(1, 256), (7, 512), (256, 512), (1000, 4096), (333, 5120)])
+@pytest.mark.parametrize("M,H", [(1, 256), (7, 512), (256, 512), (1000, 4096), (333, 5120),
+                                 (37, 33024), (5, 65536)])
 def test_rmsnorm_parity(M, H):
+    """Includes rows wider than 32768 columns (one warp per row, eight values
+    per lane, the row read twice)."""
     x = syn.activation(M, H, seed=M + H, outlier_scale=20.0, device=DEV)
     gamma = (syn.normal_bf16((H,), 0.1, seed=H, tensor="w", device=DEV) + 1.0).to(torch.bfloat16)
     check_rmsnorm(x, gamma, 1e-6, f"rmsnorm {M}x{H}")
@@ -122,7 +125,7 @@ def test_rmsnorm_parity_many_rows(H):
     check_rmsnorm(x, gamma, 1e-6, f"rmsnorm {M}x{H}")
 
 
-@pytest.mark.parametrize("H", [4096, 8192, 16384, 32768])
+@pytest.mark.parametrize("H", [4096, 8192, 16384, 32768, 33024])
 def test_rmsnorm_rows_batch_invariant(H):
     """A row's bits do not depend on the batch: rows of a large batch equal
     the same rows normalised alone or in small batches (one to sixteen warps

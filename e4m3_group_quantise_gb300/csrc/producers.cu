@@ -203,11 +203,11 @@ __device__ __forceinline__ int64_t quad_first_piece(int64_t qd)
     return 16 * (qd >> 2) + (qd & 3);
 }
 
-// A row is taken by `rw` warps (rw 32 threads: thread t holds quads t,
-// t + 32 rw, ...), 8 / rw rows per block (one when rw > 4); each thread holds
-// at most JQ quads, so the row is read from memory once.  (With one quad per
-// thread, capped at 64 registers: more resident warps hide the loads better
-// than a larger register budget; measured.)
+// A row is taken by `rw` warps (32 rw threads: thread t holds quads t,
+// t + 32 rw, ...), 8 / rw rows per block (integer division; one when rw > 4);
+// each thread holds at most JQ quads, so the row is read from memory once.
+// (With one quad per thread, capped at 64 registers: more resident warps hide
+// the loads better than a larger register budget; measured.)
 template <int JQ>
 __global__ void __launch_bounds__(RN_MAX_THREADS, JQ == 1 ? 2 : 1)
 rmsnorm_quantize_kernel(const uint4 *__restrict__ x, const uint4 *__restrict__ gamma, float eps, int64_t M,

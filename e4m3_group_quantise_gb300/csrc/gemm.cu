@@ -183,8 +183,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 }
 
 // 16x256b TMEM loads of 64 or 32 columns, chosen by the register array
-__device__ __forceinline__ void tmem_ld_quads(uint32_t taddr, uint32_t (&r)[32]) { ptx::tmem_ld_16x256b_x8(taddr, r); }
-__device__ __forceinline__ void tmem_ld_quads(uint32_t taddr, uint32_t (&r)[16]) { ptx::tmem_ld_16x256b_x4(taddr, r); }
 
 template <int BN, int STAGES, bool SB_PER_COLUMN, bool HALF_A>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
@@ -632,26 +630,22 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                         const float v = scur[quarter * 32 + 8 * k + (lane >> 2)];
                         sa2[k] = ptx::pack_f32x2(v, v);
                     }
-                    uint32_t q0[NPS][16], q1[NPS][16];   // lanes 0-15 and 16-31 of the quarter
-                    tmem_ld_quads(taddr, q0[0]);
-                    tmem_ld_quads(taddr + (16u << 16), q1[0]);
 #pragma unroll
                     for (int j = 0; j < NPS; ++j) {
-                        ptx::tmem_ld_wait(q0[j]);
-                        ptx::tmem_ld_wait(q1[j]);
-                        // this slab's column-scale pairs, read before the next
-                        // slab's TMEM loads are issued: a shared load queued
-                        // behind a pending TMEM load waits for it (+2.8 % on
-                        // the 256-wide tiles)
+                        // the slab's partials (lanes 0-15 and 16-31 of the
+                        // quarter), loaded and waited for as packed column pairs:
+                        // +7 % against loads into loose 32-bit registers issued a
+                        // slab ahead, whose pairs had to be moved together before
+                        // every packed multiply-add (and a wait drains every
+                        // pending load anyway)
+                        uint64_t p0[8], p1[8];
+                        ptx::tmem_ld_16x256b_x4_pair_packed(taddr + j * 8 * PS, p0, p1);
+                        // this slab's column-scale pairs (read with no TMEM load
+                        // pending: a shared load queued behind one waits for it)
                         uint64_t sb2[PS];
 #pragma unroll
                         for (int i = 0; i < PS; ++i)
                             sb2[i] = *reinterpret_cast<const uint64_t *>(sbcol + 8 * (j * PS + i) + cq);
-                        if (j + 1 < NPS) {
-                            tmem_ld_quads(taddr + (j + 1) * 8 * PS, q0[j + 1]);
-                            tmem_ld_quads(taddr + (16u << 16) + (j + 1) * 8 * PS, q1[j + 1]);
-                        }
-                        const uint32_t *p0 = q0[j], *p1 = q1[j];
                         if (j + 1 == NPS) {
                             // the whole partial is in registers: hand the buffer back
                             ptx::tc_fence_before();
@@ -663,9 +657,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                             const int b = j * PS + i;
 #pragma unroll
                             for (int k = 0; k < 4; ++k) {
-                                const uint32_t *p = (k < 2 ? p0 : p1) + 4 * i + 2 * (k & 1);
+                                const uint64_t pp = (k < 2 ? p0 : p1)[2 * i + (k & 1)];
                                 const uint64_t w = ptx::mul_f32x2(sa2[k], sb2[i]);
-                                ptx::fma_f32x2(accp[k * CB + b], ptx::pack_f32x2(p[0], p[1]), w);
+                                ptx::fma_f32x2(accp[k * CB + b], pp, w);
                             }
                         }
                     }
@@ -675,32 +669,32 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                     // per wait where the range allows (against two 32-column
                     // loads: +1.5 %), so each group pays the TMEM load latency
                     // only COLS_PER_WG / 64 times
-                    auto apply32 = [&](const uint32_t(&p)[32], const int c0) {
+                    auto apply32 = [&](const uint64_t *p, const int c0) {
                         const uint64_t w2 = ptx::pack_f32x2(w_blk, w_blk);
                         uint64_t *a0 = acc2 + c0 / 2;
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
-                            ptx::fma_f32x2(a0[i], ptx::pack_f32x2(p[2 * i], p[2 * i + 1]), w2);
+                            ptx::fma_f32x2(a0[i], p[i], w2);
                     };
+                    // partials loaded and waited for as packed column pairs
+                    // (no moves to pair loose registers before each multiply-add)
                     if (LPW == 2) {
 #pragma unroll
                         for (int h = 0; h < CHUNKS / 2; ++h) {
-                            uint32_t pp[64];
-                            ptx::tmem_ld_32x32b_x64(taddr + h * 64, pp);
-                            ptx::tmem_ld_wait(pp);
+                            uint64_t pp[32];
+                            ptx::tmem_ld_32x32b_x64_packed(taddr + h * 64, pp);
                             if (h + 1 == CHUNKS / 2) {
                                 // the whole partial is in registers: hand the buffer back
                                 ptx::tc_fence_before();
                                 __syncwarp();
                                 ptx::mbar_arrive_elected(&tempty[buf]);
                             }
-                            apply32(*reinterpret_cast<const uint32_t(*)[32]>(pp), h * 64);
-                            apply32(*reinterpret_cast<const uint32_t(*)[32]>(pp + 32), h * 64 + 32);
+                            apply32(pp, h * 64);
+                            apply32(pp + 16, h * 64 + 32);
                         }
                     } else {
-                        uint32_t p0[32];
-                        ptx::tmem_ld_32x32b_x32(taddr, p0);
-                        ptx::tmem_ld_wait(p0);
+                        uint64_t p0[16];
+                        ptx::tmem_ld_32x32b_x32_packed(taddr, p0);
                         ptx::tc_fence_before();
                         __syncwarp();
                         ptx::mbar_arrive_elected(&tempty[buf]);

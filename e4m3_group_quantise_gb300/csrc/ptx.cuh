@@ -318,121 +318,138 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar)
                  : "memory");
 }
 
-// 32 lanes x 32 columns of 32-bit data: thread i of the warp receives lane
-// (base lane + i), columns col..col+31.  Completion is NOT waited for here.
-__device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32])
+// Loads that are waited for inside the same asm statement, their 32-bit
+// results handed out as packed pairs of adjacent columns (64-bit registers):
+// the register allocator then places each pair in an aligned register pair
+// once, instead of moving two loose registers into one before every packed
+// multiply-add (measured on the per-column Wgrad promotion: +7 %).
+//
+// Lanes 0-15 (a, at taddr) and 16-31 (b, at taddr + 16 lanes) of a 32-lane
+// quarter, 16x256b.x4 each (32 columns): thread t receives, for each 8-column
+// block j, lanes (base + t/4) and (base + 8 + t/4) at columns 8j + 2(t%4) and
+// 8j + 2(t%4) + 1 -- pair 2j from the first lane, pair 2j + 1 from the second.
+// A thread thus holds four rows of the quarter (t/4, 8 + t/4, 16 + t/4 and
+// 24 + t/4) at a quarter of its columns.
+__device__ __forceinline__ void tmem_ld_16x256b_x4_pair_packed(uint32_t taddr, uint64_t (&a)[8], uint64_t (&b)[8])
 {
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
-          "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
-          "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
-          "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        "{\n\t"
+        ".reg .b32 t0, t1, t2, t3, t4, t5, t6, t7, t8, t9, t10, t11, t12, t13, t14, t15;\n\t"
+        ".reg .b32 u0, u1, u2, u3, u4, u5, u6, u7, u8, u9, u10, u11, u12, u13, u14, u15;\n\t"
+        "tcgen05.ld.sync.aligned.16x256b.x4.b32 {t0, t1, t2, t3, t4, t5, t6, t7, t8, t9, t10, t11, t12, t13, t14, t15}, [%16];\n\t"
+        "tcgen05.ld.sync.aligned.16x256b.x4.b32 {u0, u1, u2, u3, u4, u5, u6, u7, u8, u9, u10, u11, u12, u13, u14, u15}, [%17];\n\t"
+        "tcgen05.wait::ld.sync.aligned;\n\t"
+        "mov.b64 %0, {t0, t1};\n\t"
+        "mov.b64 %1, {t2, t3};\n\t"
+        "mov.b64 %2, {t4, t5};\n\t"
+        "mov.b64 %3, {t6, t7};\n\t"
+        "mov.b64 %4, {t8, t9};\n\t"
+        "mov.b64 %5, {t10, t11};\n\t"
+        "mov.b64 %6, {t12, t13};\n\t"
+        "mov.b64 %7, {t14, t15};\n\t"
+        "mov.b64 %8, {u0, u1};\n\t"
+        "mov.b64 %9, {u2, u3};\n\t"
+        "mov.b64 %10, {u4, u5};\n\t"
+        "mov.b64 %11, {u6, u7};\n\t"
+        "mov.b64 %12, {u8, u9};\n\t"
+        "mov.b64 %13, {u10, u11};\n\t"
+        "mov.b64 %14, {u12, u13};\n\t"
+        "mov.b64 %15, {u14, u15};\n\t"
+        "}"
+        : "=l"(a[0]), "=l"(a[1]), "=l"(a[2]), "=l"(a[3]), "=l"(a[4]), "=l"(a[5]), "=l"(a[6]), "=l"(a[7]),
+          "=l"(b[0]), "=l"(b[1]), "=l"(b[2]), "=l"(b[3]), "=l"(b[4]), "=l"(b[5]), "=l"(b[6]), "=l"(b[7])
+        : "r"(taddr), "r"(taddr + (16u << 16))
+        : "memory");
+}
+
+// 32 lanes x 64 columns (32x32b.x64), waited for: thread i of the warp
+// receives TMEM lane (base lane + i), pair k = columns 2k, 2k+1.
+__device__ __forceinline__ void tmem_ld_32x32b_x64_packed(uint32_t taddr, uint64_t (&r)[32])
+{
+    asm volatile(
+        "{\n\t"
+        ".reg .b32 t0, t1, t2, t3, t4, t5, t6, t7, t8, t9, t10, t11, t12, t13, t14, t15,"
+        " t16, t17, t18, t19, t20, t21, t22, t23, t24, t25, t26, t27, t28, t29, t30, t31,"
+        " t32, t33, t34, t35, t36, t37, t38, t39, t40, t41, t42, t43, t44, t45, t46, t47,"
+        " t48, t49, t50, t51, t52, t53, t54, t55, t56, t57, t58, t59, t60, t61, t62, t63;\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {t0, t1, t2, t3, t4, t5, t6, t7, t8, t9, t10, t11, t12, t13, t14, t15,"
+        " t16, t17, t18, t19, t20, t21, t22, t23, t24, t25, t26, t27, t28, t29, t30, t31,"
+        " t32, t33, t34, t35, t36, t37, t38, t39, t40, t41, t42, t43, t44, t45, t46, t47,"
+        " t48, t49, t50, t51, t52, t53, t54, t55, t56, t57, t58, t59, t60, t61, t62, t63}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;\n\t"
+        "mov.b64 %0, {t0, t1};\n\t"
+        "mov.b64 %1, {t2, t3};\n\t"
+        "mov.b64 %2, {t4, t5};\n\t"
+        "mov.b64 %3, {t6, t7};\n\t"
+        "mov.b64 %4, {t8, t9};\n\t"
+        "mov.b64 %5, {t10, t11};\n\t"
+        "mov.b64 %6, {t12, t13};\n\t"
+        "mov.b64 %7, {t14, t15};\n\t"
+        "mov.b64 %8, {t16, t17};\n\t"
+        "mov.b64 %9, {t18, t19};\n\t"
+        "mov.b64 %10, {t20, t21};\n\t"
+        "mov.b64 %11, {t22, t23};\n\t"
+        "mov.b64 %12, {t24, t25};\n\t"
+        "mov.b64 %13, {t26, t27};\n\t"
+        "mov.b64 %14, {t28, t29};\n\t"
+        "mov.b64 %15, {t30, t31};\n\t"
+        "mov.b64 %16, {t32, t33};\n\t"
+        "mov.b64 %17, {t34, t35};\n\t"
+        "mov.b64 %18, {t36, t37};\n\t"
+        "mov.b64 %19, {t38, t39};\n\t"
+        "mov.b64 %20, {t40, t41};\n\t"
+        "mov.b64 %21, {t42, t43};\n\t"
+        "mov.b64 %22, {t44, t45};\n\t"
+        "mov.b64 %23, {t46, t47};\n\t"
+        "mov.b64 %24, {t48, t49};\n\t"
+        "mov.b64 %25, {t50, t51};\n\t"
+        "mov.b64 %26, {t52, t53};\n\t"
+        "mov.b64 %27, {t54, t55};\n\t"
+        "mov.b64 %28, {t56, t57};\n\t"
+        "mov.b64 %29, {t58, t59};\n\t"
+        "mov.b64 %30, {t60, t61};\n\t"
+        "mov.b64 %31, {t62, t63};\n\t"
+        "}"
+        : "=l"(r[0]), "=l"(r[1]), "=l"(r[2]), "=l"(r[3]), "=l"(r[4]), "=l"(r[5]), "=l"(r[6]), "=l"(r[7]),
+          "=l"(r[8]), "=l"(r[9]), "=l"(r[10]), "=l"(r[11]), "=l"(r[12]), "=l"(r[13]), "=l"(r[14]), "=l"(r[15]),
+          "=l"(r[16]), "=l"(r[17]), "=l"(r[18]), "=l"(r[19]), "=l"(r[20]), "=l"(r[21]), "=l"(r[22]), "=l"(r[23]),
+          "=l"(r[24]), "=l"(r[25]), "=l"(r[26]), "=l"(r[27]), "=l"(r[28]), "=l"(r[29]), "=l"(r[30]), "=l"(r[31])
         : "r"(taddr)
         : "memory");
 }
 
-// 16 lanes x 256 bits, repeated along the columns (x8: 64 columns, x4: 32).
-// Thread t receives, for each 8-column block j of the range, lanes
-// (base + t/4) and (base + 8 + t/4) at columns 8j + 2(t%4) and 8j + 2(t%4) + 1:
-// r[4j], r[4j+1] from the first lane, r[4j+2], r[4j+3] from the second.  A
-// thread thus holds four rows of a 32-lane quarter (two loads, bases 0 and
-// 16) but only a quarter of its columns.  Completion is NOT waited for here.
-__device__ __forceinline__ void tmem_ld_16x256b_x8(uint32_t taddr, uint32_t (&r)[32])
+// 32 lanes x 32 columns (32x32b.x32), waited for: thread i of the warp
+// receives TMEM lane (base lane + i), pair k = columns 2k, 2k+1.
+__device__ __forceinline__ void tmem_ld_32x32b_x32_packed(uint32_t taddr, uint64_t (&r)[16])
 {
     asm volatile(
-        "tcgen05.ld.sync.aligned.16x256b.x8.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
-          "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
-          "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
-          "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        "{\n\t"
+        ".reg .b32 t0, t1, t2, t3, t4, t5, t6, t7, t8, t9, t10, t11, t12, t13, t14, t15,"
+        " t16, t17, t18, t19, t20, t21, t22, t23, t24, t25, t26, t27, t28, t29, t30, t31;\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {t0, t1, t2, t3, t4, t5, t6, t7, t8, t9, t10, t11, t12, t13, t14, t15,"
+        " t16, t17, t18, t19, t20, t21, t22, t23, t24, t25, t26, t27, t28, t29, t30, t31}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;\n\t"
+        "mov.b64 %0, {t0, t1};\n\t"
+        "mov.b64 %1, {t2, t3};\n\t"
+        "mov.b64 %2, {t4, t5};\n\t"
+        "mov.b64 %3, {t6, t7};\n\t"
+        "mov.b64 %4, {t8, t9};\n\t"
+        "mov.b64 %5, {t10, t11};\n\t"
+        "mov.b64 %6, {t12, t13};\n\t"
+        "mov.b64 %7, {t14, t15};\n\t"
+        "mov.b64 %8, {t16, t17};\n\t"
+        "mov.b64 %9, {t18, t19};\n\t"
+        "mov.b64 %10, {t20, t21};\n\t"
+        "mov.b64 %11, {t22, t23};\n\t"
+        "mov.b64 %12, {t24, t25};\n\t"
+        "mov.b64 %13, {t26, t27};\n\t"
+        "mov.b64 %14, {t28, t29};\n\t"
+        "mov.b64 %15, {t30, t31};\n\t"
+        "}"
+        : "=l"(r[0]), "=l"(r[1]), "=l"(r[2]), "=l"(r[3]), "=l"(r[4]), "=l"(r[5]), "=l"(r[6]), "=l"(r[7]),
+          "=l"(r[8]), "=l"(r[9]), "=l"(r[10]), "=l"(r[11]), "=l"(r[12]), "=l"(r[13]), "=l"(r[14]), "=l"(r[15])
         : "r"(taddr)
         : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld_16x256b_x4(uint32_t taddr, uint32_t (&r)[16])
-{
-    asm volatile(
-        "tcgen05.ld.sync.aligned.16x256b.x4.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
-          "=r"(r[15])
-        : "r"(taddr)
-        : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[16])
-{
-    asm volatile("tcgen05.wait::ld.sync.aligned;"
-                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
-                   "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
-                   "+r"(r[14]), "+r"(r[15])
-                 :
-                 : "memory");
-}
-
-// 32 lanes x 64 columns: thread i receives lane (base + i), columns
-// col..col+63 (one instruction for what two x32 loads would fetch).
-__device__ __forceinline__ void tmem_ld_32x32b_x64(uint32_t taddr, uint32_t (&r)[64])
-{
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {"
-        "%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, "
-        "%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, "
-        "%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
-          "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
-          "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
-          "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
-          "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
-        : "r"(taddr)
-        : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[64])
-{
-    asm volatile("tcgen05.wait::ld.sync.aligned;"
-                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
-                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]),
-                   "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
-                   "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]),
-                   "+r"(r[32]), "+r"(r[33]), "+r"(r[34]), "+r"(r[35]), "+r"(r[36]), "+r"(r[37]), "+r"(r[38]), "+r"(r[39]),
-                   "+r"(r[40]), "+r"(r[41]), "+r"(r[42]), "+r"(r[43]), "+r"(r[44]), "+r"(r[45]), "+r"(r[46]), "+r"(r[47]),
-                   "+r"(r[48]), "+r"(r[49]), "+r"(r[50]), "+r"(r[51]), "+r"(r[52]), "+r"(r[53]), "+r"(r[54]), "+r"(r[55]),
-                   "+r"(r[56]), "+r"(r[57]), "+r"(r[58]), "+r"(r[59]), "+r"(r[60]), "+r"(r[61]), "+r"(r[62]), "+r"(r[63])
-                 :
-                 : "memory");
-}
-
-// Wait for this thread's outstanding tcgen05.ld; the registers are passed
-// through so that no use of them can be scheduled before the wait.
-__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32])
-{
-    asm volatile("tcgen05.wait::ld.sync.aligned;"
-                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
-                   "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
-                   "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]),
-                   "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]),
-                   "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
-                 :
-                 : "memory");
-}
-
-// Waits for every tcgen05.ld of this thread (registers already consumed or discarded).
-__device__ __forceinline__ void tmem_ld_wait_all()
-{
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
 // Shared-memory matrix descriptor for a K-major operand tile stored with the

@@ -72,20 +72,20 @@ FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1
 # SHA-256 is recorded here (the kernel and its inline-PTX helpers) and is
 # reported as null once they differ.
 GEMM_TRAFFIC = {"per_launch_bytes": {
-                                     "dgrad:down": 635900416,
-                                     "dgrad:gate_up": 2344995840,
-                                     "dgrad:o": 172978688,
-                                     "dgrad:qkv": 222512128,
-                                     "fprop:down": 666591488,
-                                     "fprop:gate_up": 1331336704,
-                                     "fprop:o": 174819584,
-                                     "fprop:qkv": 254374912,
-                                     "wgrad:down": 934543872,
-                                     "wgrad:gate_up": 2348488192,
-                                     "wgrad:o": 306686208,
-                                     "wgrad:qkv": 483127552},
+                                     "dgrad:down": 635139072,
+                                     "dgrad:gate_up": 2345906688,
+                                     "dgrad:o": 173090560,
+                                     "dgrad:qkv": 222621440,
+                                     "fprop:down": 673834496,
+                                     "fprop:gate_up": 1326319104,
+                                     "fprop:o": 174941184,
+                                     "fprop:qkv": 254525696,
+                                     "wgrad:down": 936477696,
+                                     "wgrad:gate_up": 2336228864,
+                                     "wgrad:o": 307261184,
+                                     "wgrad:qkv": 482988544},
                 "sources": ("gemm.cu", "ptx.cuh"),
-                "sha256": "810dd5c2a92e557fff4058aeb4747920215b59d1f729c3eeb46f85282b8c0ad3"}
+                "sha256": "19c236778fab4510e4c7b71a3a1d10939e4ca574810520581990a83271d863e3"}
 
 
 def gemm_sources_sha256() -> str:
